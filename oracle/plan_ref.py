@@ -1,0 +1,220 @@
+"""Plain restatement of the planner's partition rules (TEST INFRASTRUCTURE).
+
+The timing script of the FlashInfer issue "How are prefill and decode kernels
+different?" builds "auxiliary data structures" once per batch
+(``begin_forward`` on the indptr arrays) into a caller-owned workspace and
+then calls ``forward`` many times.  The library's planner does the same: it
+turns the CSR page table into a list of work items and a merge map.  This
+module states those rules a second time, in Python, so that the metadata the
+C++ planner writes can be compared with it bit for bit.
+
+Rules (the planner is deterministic; nothing depends on timing):
+
+1. Per request: qo_b, pages_b, kv_b = (pages_b - 1) * page_size + last_b
+   (see ``oracle.attention.kv_len_of``), page_start_b.
+2. A request with qo_b == 1 goes to the decode kernel when G = Hq/Hkv is one
+   of 1, 2, 4, 8 (and ``force_prefill`` is off); every other request with
+   qo_b >= 1 goes to the tensor-core prefill kernel.
+3. Decode split ("kv-parallelism", the split-k of the same issue): with
+   P_dec = sum over decode requests of pages_b * Hkv and
+   target = 4 * num_sms, the chunk is
+   clamp(ceil(P_dec / target), max(1, 256 // page_size), max(1, 2048 // page_size))
+   pages (or the override).  Request b is cut into ceil(pages_b / chunk)
+   splits at page boundaries, for every kv head.
+4. Prefill tiles: 128 packed rows = (128 / G) query tokens x G heads.  Tile
+   [t0, t0 + n) of request b needs keys [0, e) with e = kv_b - qo_b + t0 + n
+   (causal) or kv_b; that is ceil(e / 128) key tiles of 128.  With W = the
+   sum of key tiles over all (tile, kv head) items and target = 2 * num_sms,
+   the chunk is max(8, ceil(W / target)) key tiles (or the override); an item
+   with more key tiles is cut into ceil(tiles / chunk) splits.
+5. Partial rows (fp32, in the workspace) are handed out in emission order:
+   decode splits first (request, then kv head), then prefill splits (request,
+   tile, kv head); a split group of S splits and R rows per split takes S * R
+   consecutive rows.  One merge entry is emitted per (query token, kv head)
+   of a split group: {out_row0, part_row0, nsplit, split_stride}.
+6. Items are then ordered by decreasing key count (longest first), ties in
+   emission order (a stable sort), so that the hardware's in-order block
+   dispatch spreads the long items first.
+
+Metadata layout (int32 words, every region 256-byte aligned), which is what
+``pagedattn_debug_plan_dump`` returns and ``pagedattn_plan`` copies to the
+start of the workspace:
+
+    header[64]  magic 0x50414731, version 1, B, Hq, Hkv, D, page_size,
+                num_pages, dtype, causal, T, nnz, n_dec, n_pre, n_merge,
+                n_part_rows, dec_chunk_pages, pre_chunk_tiles, num_sms, G,
+                off_pages, off_req, off_dec, off_pre, off_merge, blob_bytes,
+                off_part_o, off_part_lse, total_bytes, 0..., [32] status word
+    pages[nnz]       copy of kv_page_indices
+    req[B][4]        qo_start, qo_len, kv_len, page_start
+    dec[n_dec][8]    req, kv_head, tok0, tok1, part_row(-1 = direct), 0, 0, 0
+    pre[n_pre][8]    req, kv_head, q_tok0, q_ntok, kv_tok0, kv_tok1, part_row, 0
+    merge[n][4]      out_row0, part_row0, nsplit, split_stride
+"""
+from __future__ import annotations
+
+import numpy as np
+
+from .attention import PlanError, request_lengths
+
+MAGIC = 0x50414731
+VERSION = 1
+HDR_WORDS = 64
+STATUS_WORD = 32
+Q_ROWS = 128       # packed query rows per prefill tile
+KV_TILE = 128      # keys per prefill key tile
+DEC_ITEMS_PER_SM = 4
+PRE_ITEMS_PER_SM = 2
+PRE_MIN_CHUNK_TILES = 8
+DECODE_GROUPS = (1, 2, 4, 8)
+
+FP16, BF16 = 0, 1
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED = 0, 1, 2
+
+
+class Unsupported(ValueError):
+    pass
+
+
+def _cdiv(a, b):
+    return -(-a // b)
+
+
+def _align(x, a=256):
+    return _cdiv(x, a) * a
+
+
+def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_heads,
+          num_kv_heads, head_dim, page_size, num_pages, dtype=BF16, causal=True, num_sms=148,
+          force_prefill=False, decode_chunk_pages=0, prefill_chunk_tiles=0):
+    """Return the metadata blob (np.int32) the planner must produce."""
+    Hq, Hkv, D, ps = int(num_qo_heads), int(num_kv_heads), int(head_dim), int(page_size)
+    if Hq < 1 or Hkv < 1 or Hq % Hkv:
+        raise PlanError("num_qo_heads must be a positive multiple of num_kv_heads")
+    G = Hq // Hkv
+    if D not in (64, 128):
+        raise Unsupported("head_dim")
+    if ps < 1 or ps > 128 or (ps & (ps - 1)):
+        raise Unsupported("page_size")
+    if dtype not in (FP16, BF16):
+        raise Unsupported("dtype")
+    if Q_ROWS % G:
+        raise Unsupported("group size must divide 128")
+    if num_sms < 1:
+        raise PlanError("num_sms")
+    lens = request_lengths(qo_indptr, kv_page_indptr, kv_last_page_len, ps)
+    B = len(lens)
+    indices = np.asarray(kv_page_indices, np.int64)
+    nnz = int(np.asarray(kv_page_indptr)[-1])
+    if len(indices) < nnz:
+        raise PlanError("kv_page_indices shorter than kv_page_indptr[B]")
+    indices = indices[:nnz]
+    if nnz and (indices.min() < 0 or indices.max() >= num_pages):
+        raise PlanError("page id out of range")
+    for (qo, kv, _, _) in lens:
+        if qo > 0 and (kv < 1 or (causal and qo > kv)):
+            raise PlanError("query rows without keys")
+    T = int(np.asarray(qo_indptr)[-1])
+
+    is_dec = [qo == 1 and G in DECODE_GROUPS and not force_prefill for (qo, _, _, _) in lens]
+
+    # -- decode items (rule 3)
+    p_dec = sum(l[3] * Hkv for l, d in zip(lens, is_dec) if d)
+    lo, hi = max(1, 256 // ps), max(1, 2048 // ps)
+    chunk = decode_chunk_pages if decode_chunk_pages > 0 else min(max(_cdiv(p_dec, DEC_ITEMS_PER_SM * num_sms), lo), hi)
+    part = 0
+    dec, merges = [], []
+    for b, ((qo, kv, p0, npg), d) in enumerate(zip(lens, is_dec)):
+        if not d:
+            continue
+        ns = _cdiv(npg, chunk)
+        for h in range(Hkv):
+            base = part if ns > 1 else -1
+            if ns > 1:
+                part += ns * G
+                qs = int(qo_indptr[b])
+                merges.append((qs * Hq + h * G, base, ns, G))
+            for s in range(ns):
+                t0 = s * chunk * ps
+                t1 = min((s + 1) * chunk * ps, kv)
+                dec.append((b, h, t0, t1, base + s * G if ns > 1 else -1))
+
+    # -- prefill items (rule 4)
+    tq = Q_ROWS // G
+    tiles = []  # (b, t0, n, e)
+    for b, ((qo, kv, p0, npg), d) in enumerate(zip(lens, is_dec)):
+        if d or qo == 0:
+            continue
+        for t0 in range(0, qo, tq):
+            n = min(tq, qo - t0)
+            e = kv - qo + t0 + n if causal else kv
+            tiles.append((b, t0, n, e))
+    W = sum(_cdiv(e, KV_TILE) for (_, _, _, e) in tiles) * Hkv
+    ctiles = prefill_chunk_tiles if prefill_chunk_tiles > 0 else max(PRE_MIN_CHUNK_TILES, _cdiv(W, PRE_ITEMS_PER_SM * num_sms))
+    pre = []
+    for (b, t0, n, e) in tiles:
+        nt = _cdiv(e, KV_TILE)
+        ns = _cdiv(nt, ctiles)
+        qs = int(qo_indptr[b])
+        for h in range(Hkv):
+            base = part if ns > 1 else -1
+            if ns > 1:
+                part += ns * n * G
+                for t in range(n):
+                    merges.append(((qs + t0 + t) * Hq + h * G, base + t * G, ns, n * G))
+            for s in range(ns):
+                k0 = s * ctiles * KV_TILE
+                k1 = min((s + 1) * ctiles * KV_TILE, e)
+                pre.append((b, h, t0, n, k0, k1, base + s * n * G if ns > 1 else -1))
+
+    # -- longest first, stable (rule 6)
+    dec = sorted(dec, key=lambda it: -(it[3] - it[2]))
+    pre = sorted(pre, key=lambda it: -(it[5] - it[4]))
+
+    # -- layout
+    off_pages = HDR_WORDS * 4
+    off_req = _align(off_pages + 4 * nnz)
+    off_dec = _align(off_req + 16 * B)
+    off_pre = _align(off_dec + 32 * len(dec))
+    off_merge = _align(off_pre + 32 * len(pre))
+    blob_bytes = _align(off_merge + 16 * len(merges))
+    off_part_o = blob_bytes
+    off_part_lse = _align(off_part_o + 4 * D * part)
+    total = _align(off_part_lse + 4 * part)
+    if total >= 2 ** 31:
+        raise Unsupported("metadata and partial states exceed 2 GiB")
+
+    blob = np.zeros(blob_bytes // 4, np.int32)
+    hdr = [MAGIC, VERSION, B, Hq, Hkv, D, ps, num_pages, dtype, int(bool(causal)), T, nnz,
+           len(dec), len(pre), len(merges), part, chunk, ctiles, num_sms, G,
+           off_pages, off_req, off_dec, off_pre, off_merge, blob_bytes, off_part_o,
+           off_part_lse, total]
+    blob[:len(hdr)] = hdr
+    blob[off_pages // 4: off_pages // 4 + nnz] = indices
+    req = np.array([(int(qo_indptr[b]), qo, kv, p0) for b, (qo, kv, p0, _) in enumerate(lens)],
+                   np.int32).reshape(-1, 4)
+    blob[off_req // 4: off_req // 4 + 4 * B] = req.reshape(-1)
+    for j, it in enumerate(dec):
+        blob[off_dec // 4 + 8 * j: off_dec // 4 + 8 * j + 5] = it
+    for j, it in enumerate(pre):
+        blob[off_pre // 4 + 8 * j: off_pre // 4 + 8 * j + 7] = it
+    for j, it in enumerate(merges):
+        blob[off_merge // 4 + 4 * j: off_merge // 4 + 4 * j + 4] = it
+    return blob
+
+
+def decode_header(blob: np.ndarray) -> dict:
+    names = ["magic", "version", "B", "Hq", "Hkv", "D", "page_size", "num_pages", "dtype",
+             "causal", "T", "nnz", "n_dec", "n_pre", "n_merge", "n_part_rows", "dec_chunk_pages",
+             "pre_chunk_tiles", "num_sms", "G", "off_pages", "off_req", "off_dec", "off_pre",
+             "off_merge", "blob_bytes", "off_part_o", "off_part_lse", "total_bytes"]
+    return {n: int(blob[i]) for i, n in enumerate(names)}
+
+
+def items(blob: np.ndarray):
+    """(decode items [n,8], prefill items [n,8], merge entries [n,4]) views."""
+    h = decode_header(blob)
+    dec = blob[h["off_dec"] // 4: h["off_dec"] // 4 + 8 * h["n_dec"]].reshape(-1, 8)
+    pre = blob[h["off_pre"] // 4: h["off_pre"] // 4 + 8 * h["n_pre"]].reshape(-1, 8)
+    mer = blob[h["off_merge"] // 4: h["off_merge"] // 4 + 4 * h["n_merge"]].reshape(-1, 4)
+    return dec, pre, mer
