@@ -1,0 +1,56 @@
+// Host-side internals shared by the planner, the C ABI and the launchers.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <string>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "../../include/pagedattn.h"
+
+namespace pa {
+
+// Planner result: the metadata blob (int32 words, the exact bytes copied to
+// the start of the workspace) plus the sizes the launchers need.
+struct HostPlan {
+  std::vector<int32_t> blob;
+  int32_t B = 0, Hq = 0, Hkv = 0, D = 0, ps = 0, num_pages = 0, dtype = 0, causal = 1, T = 0, nnz = 0;
+  int32_t n_dec = 0, n_pre = 0, n_merge = 0, n_part = 0, G = 1, num_sms = 0;
+  size_t blob_bytes = 0, off_part_o = 0, off_part_lse = 0, total_bytes = 0;
+  size_t off_pages = 0, off_req = 0, off_dec = 0, off_pre = 0, off_merge = 0;
+  std::vector<int64_t> kv_len;  // per request (debug gather sizes)
+};
+
+struct PlanInputs {
+  const int32_t* qo_indptr;
+  const int32_t* kv_page_indptr;
+  const int32_t* kv_page_indices;
+  const int32_t* kv_last_page_len;
+  int32_t B, Hq, Hkv, D, ps, num_pages, dtype, causal;
+  int32_t num_sms, force_prefill, decode_chunk_pages, prefill_chunk_tiles;
+};
+
+// Validate and partition; on failure returns the status and fills `err`.
+pagedattn_status build_plan(const PlanInputs& in, HostPlan* out, std::string* err);
+
+// Launchers (one per kernel family).  All are asynchronous on `stream`.
+struct RunArgs {
+  const HostPlan* hp;
+  void* workspace;  // device base of the metadata
+  const void* q;
+  const void* kv;
+  void* out;
+  float* lse;
+  cudaStream_t stream;
+  int force_cp_async;
+};
+
+cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128);
+cudaError_t launch_decode(const RunArgs& a, const CUtensorMap* map_rows);
+cudaError_t launch_merge(const RunArgs& a);
+cudaError_t launch_debug_gather(const RunArgs& a, int32_t* page_out, int32_t* slot_out);
+
+}  // namespace pa

@@ -1,0 +1,236 @@
+// Host planner: validates one batch's page table and cuts it into work items.
+//
+// The FlashInfer issue "How are prefill and decode kernels different?"
+// builds "auxiliary data structures" once per batch (begin_forward on the
+// indptr arrays) and reuses them for many forward calls; this is that step.
+// Rules (deterministic, no dependence on timing):
+//
+//  1. Per request b: qo_b = qo_indptr[b+1] - qo_indptr[b], pages_b likewise,
+//     kv_b = (pages_b - 1) * page_size + last_b (every page full except the
+//     last, 1 <= last <= page_size as the timing script's comment requires).
+//  2. qo_b == 1 with group size G = Hq/Hkv in {1, 2, 4, 8} -> decode kernel
+//     (CUDA cores); every other request with rows -> tensor-core prefill.
+//  3. Decode split ("kv-parallelism" / split-k in the same issue): chunk =
+//     clamp(ceil(P_dec / (4 * SMs)), 256 keys, 2048 keys) in whole pages,
+//     P_dec = sum of decode pages x Hkv.  Each (request, kv head) is cut at
+//     multiples of the chunk.
+//  4. Prefill: tiles of 128 packed rows = 128/G tokens x G heads of one kv
+//     head (the G heads share every K/V tile load).  A tile needs keys
+//     [0, kv_b - qo_b + t0 + n) under the bottom-right causal mask; key tiles
+//     past that are never visited (the "skips the fully masked out tails" of
+//     the llama.cpp discussion "Pad for prefill stage?").  Split when the
+//     total key-tile count W exceeds 2 x SMs x chunk: chunk = max(8,
+//     ceil(W / (2 * SMs))) key tiles.
+//  5. Partial fp32 rows are numbered in emission order (decode splits, then
+//     prefill splits); one merge entry per (query token, kv head) of a
+//     split group.
+//  6. Items sorted by decreasing key count, ties in emission order, so the
+//     in-order block dispatch starts the longest items first.
+#include <algorithm>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "internal.h"
+#include "layout.h"
+
+namespace pa {
+
+namespace {
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline int64_t align256(int64_t x) { return cdiv(x, 256) * 256; }
+
+struct DecTmp { int32_t req, kvh, t0, t1, part; };
+struct PreTmp { int32_t req, kvh, qt0, n, k0, k1, part; };
+
+pagedattn_status fail(std::string* err, pagedattn_status s, const std::string& m) {
+  if (err) *err = m;
+  return s;
+}
+
+}  // namespace
+
+pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err) {
+  const int32_t B = in.B, Hq = in.Hq, Hkv = in.Hkv, D = in.D, ps = in.ps;
+  if (B < 0) return fail(err, PA_ERR_INVALID_ARG, "batch_size < 0");
+  if (Hq < 1 || Hkv < 1 || Hq % Hkv)
+    return fail(err, PA_ERR_INVALID_ARG, "num_qo_heads must be a positive multiple of num_kv_heads");
+  const int32_t G = Hq / Hkv;
+  if (D != 64 && D != 128) return fail(err, PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (ps < 1 || ps > 128 || (ps & (ps - 1)))
+    return fail(err, PA_ERR_UNSUPPORTED, "page_size must be a power of two in [1, 128]");
+  if (in.dtype != PA_FP16 && in.dtype != PA_BF16) return fail(err, PA_ERR_UNSUPPORTED, "dtype");
+  if (kQRows % G) return fail(err, PA_ERR_UNSUPPORTED, "group size num_qo_heads/num_kv_heads must divide 128");
+  if (in.num_sms < 1) return fail(err, PA_ERR_INVALID_ARG, "num_sms < 1");
+  if (in.num_pages < 0) return fail(err, PA_ERR_INVALID_ARG, "num_pages < 0");
+  if (!in.qo_indptr || !in.kv_page_indptr || (B > 0 && !in.kv_last_page_len))
+    return fail(err, PA_ERR_INVALID_ARG, "null host array");
+  if (in.qo_indptr[0] != 0 || in.kv_page_indptr[0] != 0)
+    return fail(err, PA_ERR_INVALID_ARG, "indptr must start at 0");
+
+  struct Req { int32_t qo, kv, p0, np; };
+  std::vector<Req> req(B);
+  for (int b = 0; b < B; ++b) {
+    const int64_t qo = int64_t(in.qo_indptr[b + 1]) - in.qo_indptr[b];
+    const int64_t np = int64_t(in.kv_page_indptr[b + 1]) - in.kv_page_indptr[b];
+    if (qo < 0 || np < 0) return fail(err, PA_ERR_INVALID_ARG, "indptr must be nondecreasing");
+    const int32_t last = in.kv_last_page_len[b];
+    if (np > 0 && (last < 1 || last > ps))
+      return fail(err, PA_ERR_INVALID_ARG,
+                  "kv_last_page_len[" + std::to_string(b) + "]=" + std::to_string(last) +
+                      " outside [1, page_size]");
+    const int64_t kv = np > 0 ? (np - 1) * ps + last : 0;
+    if (kv > INT32_MAX) return fail(err, PA_ERR_UNSUPPORTED, "kv_len exceeds int32");
+    req[b] = {int32_t(qo), int32_t(kv), in.kv_page_indptr[b], int32_t(np)};
+  }
+  const int64_t nnz = B > 0 ? in.kv_page_indptr[B] : 0;
+  if (nnz > 0 && !in.kv_page_indices) return fail(err, PA_ERR_INVALID_ARG, "null kv_page_indices");
+  for (int64_t i = 0; i < nnz; ++i) {
+    const int32_t p = in.kv_page_indices[i];
+    if (p < 0 || p >= in.num_pages)
+      return fail(err, PA_ERR_INVALID_ARG,
+                  "kv_page_indices[" + std::to_string(i) + "]=" + std::to_string(p) + " out of range");
+  }
+  for (int b = 0; b < B; ++b) {
+    if (req[b].qo > 0 && (req[b].kv < 1 || (in.causal && req[b].qo > req[b].kv)))
+      return fail(err, PA_ERR_INVALID_ARG,
+                  "request " + std::to_string(b) + " has query rows without keys (qo_len > kv_len)");
+  }
+  const int32_t T = B > 0 ? in.qo_indptr[B] : 0;
+
+  const bool dec_group = (G == 1 || G == 2 || G == 4 || G == 8);
+  std::vector<char> is_dec(B, 0);
+  for (int b = 0; b < B; ++b) is_dec[b] = (req[b].qo == 1 && dec_group && !in.force_prefill) ? 1 : 0;
+
+  // -- rule 3: decode items
+  int64_t p_dec = 0;
+  for (int b = 0; b < B; ++b)
+    if (is_dec[b]) p_dec += int64_t(req[b].np) * Hkv;
+  const int64_t lo = std::max<int64_t>(1, 256 / ps), hi = std::max<int64_t>(1, 2048 / ps);
+  int64_t chunk = in.decode_chunk_pages > 0
+                      ? in.decode_chunk_pages
+                      : std::min(std::max(cdiv(p_dec, int64_t(4) * in.num_sms), lo), hi);
+  int64_t part = 0;
+  std::vector<DecTmp> dec;
+  std::vector<MergeEntry> merges;
+  for (int b = 0; b < B; ++b) {
+    if (!is_dec[b]) continue;
+    const int64_t ns = cdiv(req[b].np, chunk);
+    for (int h = 0; h < Hkv; ++h) {
+      const int64_t base = ns > 1 ? part : -1;
+      if (ns > 1) {
+        part += ns * G;
+        merges.push_back({int32_t(int64_t(in.qo_indptr[b]) * Hq + h * G), int32_t(base), int32_t(ns), G});
+      }
+      for (int64_t s = 0; s < ns; ++s) {
+        const int64_t t0 = s * chunk * ps;
+        const int64_t t1 = std::min<int64_t>((s + 1) * chunk * ps, req[b].kv);
+        dec.push_back({b, h, int32_t(t0), int32_t(t1), ns > 1 ? int32_t(base + s * G) : -1});
+      }
+    }
+  }
+
+  // -- rule 4: prefill items
+  const int32_t tq = kQRows / G;
+  struct Tile { int32_t b, t0, n; int64_t e; };
+  std::vector<Tile> tiles;
+  for (int b = 0; b < B; ++b) {
+    if (is_dec[b] || req[b].qo == 0) continue;
+    for (int32_t t0 = 0; t0 < req[b].qo; t0 += tq) {
+      const int32_t n = std::min(tq, req[b].qo - t0);
+      const int64_t e = in.causal ? int64_t(req[b].kv) - req[b].qo + t0 + n : req[b].kv;
+      tiles.push_back({b, t0, n, e});
+    }
+  }
+  int64_t W = 0;
+  for (auto& t : tiles) W += cdiv(t.e, kKvTile);
+  W *= Hkv;
+  const int64_t ctiles = in.prefill_chunk_tiles > 0 ? in.prefill_chunk_tiles
+                                                    : std::max<int64_t>(8, cdiv(W, int64_t(2) * in.num_sms));
+  std::vector<PreTmp> pre;
+  for (auto& t : tiles) {
+    const int64_t nt = cdiv(t.e, kKvTile);
+    const int64_t ns = cdiv(nt, ctiles);
+    const int64_t qs = in.qo_indptr[t.b];
+    for (int h = 0; h < Hkv; ++h) {
+      const int64_t base = ns > 1 ? part : -1;
+      if (ns > 1) {
+        part += ns * t.n * G;
+        for (int32_t k = 0; k < t.n; ++k)
+          merges.push_back({int32_t((qs + t.t0 + k) * Hq + h * G), int32_t(base + int64_t(k) * G),
+                            int32_t(ns), int32_t(t.n * G)});
+      }
+      for (int64_t s = 0; s < ns; ++s) {
+        const int64_t k0 = s * ctiles * kKvTile;
+        const int64_t k1 = std::min<int64_t>((s + 1) * ctiles * kKvTile, t.e);
+        pre.push_back({t.b, h, t.t0, t.n, int32_t(k0), int32_t(k1),
+                       ns > 1 ? int32_t(base + s * int64_t(t.n) * G) : -1});
+      }
+    }
+  }
+  if (part > INT32_MAX / 256) return fail(err, PA_ERR_UNSUPPORTED, "too many partial rows");
+
+  // -- rule 6: longest first, stable
+  std::stable_sort(dec.begin(), dec.end(),
+                   [](const DecTmp& a, const DecTmp& b) { return (a.t1 - a.t0) > (b.t1 - b.t0); });
+  std::stable_sort(pre.begin(), pre.end(),
+                   [](const PreTmp& a, const PreTmp& b) { return (a.k1 - a.k0) > (b.k1 - b.k0); });
+
+  // -- layout
+  const int64_t off_pages = HDR_WORDS * 4;
+  const int64_t off_req = align256(off_pages + 4 * nnz);
+  const int64_t off_dec = align256(off_req + 16 * int64_t(B));
+  const int64_t off_pre = align256(off_dec + 32 * int64_t(dec.size()));
+  const int64_t off_merge = align256(off_pre + 32 * int64_t(pre.size()));
+  const int64_t blob_bytes = align256(off_merge + 16 * int64_t(merges.size()));
+  const int64_t off_part_o = blob_bytes;
+  const int64_t off_part_lse = align256(off_part_o + 4 * int64_t(D) * part);
+  const int64_t total = align256(off_part_lse + 4 * part);
+  if (total >= (int64_t(1) << 31)) return fail(err, PA_ERR_UNSUPPORTED, "metadata and partial states exceed 2 GiB");
+
+  std::vector<int32_t>& blob = hp->blob;
+  blob.assign(size_t(blob_bytes / 4), 0);
+  const int32_t hdr[] = {kMagic, kVersion, B, Hq, Hkv, D, ps, in.num_pages, in.dtype, in.causal ? 1 : 0,
+                         T, int32_t(nnz), int32_t(dec.size()), int32_t(pre.size()), int32_t(merges.size()),
+                         int32_t(part), int32_t(chunk), int32_t(ctiles), in.num_sms, G,
+                         int32_t(off_pages), int32_t(off_req), int32_t(off_dec), int32_t(off_pre),
+                         int32_t(off_merge), int32_t(blob_bytes), int32_t(off_part_o),
+                         int32_t(off_part_lse), int32_t(total)};
+  std::memcpy(blob.data(), hdr, sizeof(hdr));
+  if (nnz) std::memcpy(blob.data() + off_pages / 4, in.kv_page_indices, size_t(4 * nnz));
+  for (int b = 0; b < B; ++b) {
+    int32_t* r = blob.data() + off_req / 4 + 4 * b;
+    r[0] = in.qo_indptr[b];
+    r[1] = req[b].qo;
+    r[2] = req[b].kv;
+    r[3] = req[b].p0;
+  }
+  for (size_t j = 0; j < dec.size(); ++j) {
+    int32_t* r = blob.data() + off_dec / 4 + 8 * j;
+    r[0] = dec[j].req; r[1] = dec[j].kvh; r[2] = dec[j].t0; r[3] = dec[j].t1; r[4] = dec[j].part;
+  }
+  for (size_t j = 0; j < pre.size(); ++j) {
+    int32_t* r = blob.data() + off_pre / 4 + 8 * j;
+    r[0] = pre[j].req; r[1] = pre[j].kvh; r[2] = pre[j].qt0; r[3] = pre[j].n;
+    r[4] = pre[j].k0; r[5] = pre[j].k1; r[6] = pre[j].part;
+  }
+  for (size_t j = 0; j < merges.size(); ++j) {
+    int32_t* r = blob.data() + off_merge / 4 + 4 * j;
+    r[0] = merges[j].out_row0; r[1] = merges[j].part_row0; r[2] = merges[j].nsplit; r[3] = merges[j].split_stride;
+  }
+
+  hp->B = B; hp->Hq = Hq; hp->Hkv = Hkv; hp->D = D; hp->ps = ps; hp->num_pages = in.num_pages;
+  hp->dtype = in.dtype; hp->causal = in.causal ? 1 : 0; hp->T = T; hp->nnz = int32_t(nnz);
+  hp->n_dec = int32_t(dec.size()); hp->n_pre = int32_t(pre.size()); hp->n_merge = int32_t(merges.size());
+  hp->n_part = int32_t(part); hp->G = G; hp->num_sms = in.num_sms;
+  hp->blob_bytes = size_t(blob_bytes); hp->off_part_o = size_t(off_part_o);
+  hp->off_part_lse = size_t(off_part_lse); hp->total_bytes = size_t(total);
+  hp->off_pages = size_t(off_pages); hp->off_req = size_t(off_req); hp->off_dec = size_t(off_dec);
+  hp->off_pre = size_t(off_pre); hp->off_merge = size_t(off_merge);
+  hp->kv_len.resize(B);
+  for (int b = 0; b < B; ++b) hp->kv_len[b] = req[b].kv;
+  return PA_OK;
+}
+
+}  // namespace pa

@@ -1,0 +1,215 @@
+/*
+ * pagedattn -- batched ragged attention over a paged KV cache, for one
+ * GB300 GPU (sm_103a).  Plain C ABI: plain pointers and sizes, no C++ or
+ * framework types cross it.
+ *
+ * The problem statement follows the FlashInfer issue "How are prefill and
+ * decode kernels different?" (the timing script and its
+ * BatchDecodeWithPagedKVCacheWrapper / BatchPrefillWithPagedKVCacheWrapper
+ * calls): a batch of requests, request b owning
+ *
+ *   - qo_len_b query rows packed in q[T, Hq, D] between qo_indptr[b] and
+ *     qo_indptr[b+1] (prefill chunks have qo_len > 1, decodes qo_len = 1);
+ *   - kv_len_b keys/values stored in the pages kv_page_indices[
+ *     kv_page_indptr[b] .. kv_page_indptr[b+1]) of the cache
+ *     kv_cache[num_pages, 2, page_size, Hkv, D] ("NHD": index 0 of the
+ *     second dimension holds K, index 1 holds V); every page is full except
+ *     the last, which holds kv_last_page_len[b] slots, 1 <= last <= page_size.
+ *     kv_len_b = (pages_b - 1) * page_size + last_b.
+ *
+ * Query head h reads kv head h / (Hq / Hkv) (grouped-query attention).  Query
+ * row i of request b sits at absolute position kv_len_b - qo_len_b + i and,
+ * with causal = 1, sees keys [0, kv_len_b - qo_len_b + i] (the mask aligned
+ * to the bottom-right, so new tokens appended after a shared prefix -- the
+ * vLLM issue "Question about efficient memory sharing (prefix sharing)" --
+ * see the whole prefix, and fully masked tails are never visited, as the
+ * llama.cpp discussion "Pad for prefill stage?" describes).  With scale =
+ * 1/sqrt(D):
+ *
+ *   out[row, h, :] = sum_t softmax_t(scale * q[row,h,:] . K[t,:]) * V[t,:]
+ *   lse[row, h]    = ln sum_t exp(scale * q[row,h,:] . K[t,:])   (natural log)
+ *
+ * Several page tables may list the same physical page (prefix sharing): the
+ * library only reads the cache.
+ *
+ * Life cycle (the script's begin_forward / forward / end_forward):
+ *   pagedattn_plan()          once per batch: host work, one H2D copy
+ *   pagedattn_run()           any number of times, asynchronous, no alloc
+ *   pagedattn_plan_destroy()  when the batch is done
+ *
+ * Errors: every call returns a pagedattn_status; the text of the last error
+ * on the calling thread is pagedattn_last_error().  No call aborts, prints or
+ * throws.
+ */
+#ifndef PAGEDATTN_H_
+#define PAGEDATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PAGEDATTN_API __attribute__((visibility("default")))
+#else
+#define PAGEDATTN_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* CUDA stream handle, identical to cudaStream_t (a CUstream_st pointer). */
+typedef struct CUstream_st* pagedattn_stream_t;
+
+typedef struct pagedattn_plan_s* pagedattn_plan_t; /* opaque, owned by the library */
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,         /* malformed indptr / page ids / lengths / pointers  */
+  PA_ERR_UNSUPPORTED = 2,         /* head_dim, page_size, dtype or group size not built */
+  PA_ERR_WORKSPACE_TOO_SMALL = 3, /* workspace_bytes < pagedattn_workspace_size()       */
+  PA_ERR_CUDA = 4,                /* a CUDA runtime call failed (message has the code)  */
+  PA_ERR_DEVICE_CHECK = 5,        /* an in-kernel check fired (see device_status)       */
+  PA_ERR_TIMEOUT = 6              /* an in-kernel wait gave up after its bound          */
+} pagedattn_status;
+
+typedef enum { PA_FP16 = 0, PA_BF16 = 1 } pagedattn_dtype;
+
+/* Optional planner settings; pass NULL for the defaults (all zero). */
+typedef struct {
+  int32_t num_sms;             /* SMs to plan for; 0 = ask the current device        */
+  int32_t force_prefill;       /* 1: qo_len == 1 requests use the tensor-core kernel */
+  int32_t decode_chunk_pages;  /* > 0: pages per decode split (default: see plan)    */
+  int32_t prefill_chunk_tiles; /* > 0: 128-key tiles per prefill split               */
+  int32_t force_cp_async;      /* 1: stage prefill K/V with cp.async instead of TMA   */
+  int32_t reserved[3];         /* must be 0                                          */
+} pagedattn_options;
+
+/* Stage bits for pagedattn_run_stages. */
+#define PA_STAGE_PREFILL 1u
+#define PA_STAGE_DECODE 2u
+#define PA_STAGE_MERGE 4u
+#define PA_STAGE_ALL 7u
+
+/* Status bits the kernels OR into the device status word. */
+#define PA_DEV_TIMEOUT 1
+#define PA_DEV_BAD_INDEX 2
+
+/*
+ * Build the work partition for one batch ("auxiliary data structures" that
+ * begin_forward builds, in the timing script).
+ *
+ * qo_indptr        host, int32[batch_size + 1], [0] == 0, nondecreasing.
+ * kv_page_indptr   host, int32[batch_size + 1], [0] == 0, nondecreasing.
+ * kv_page_indices  host, int32[kv_page_indptr[batch_size]], each in [0, num_pages).
+ * kv_last_page_len host, int32[batch_size], in [1, page_size] for every request
+ *                  that has pages.
+ * num_qo_heads, num_kv_heads: num_qo_heads a positive multiple of num_kv_heads;
+ *                  the group size num_qo_heads / num_kv_heads must divide 128.
+ * head_dim         64 or 128.  page_size: a power of two in [1, 128].
+ * causal           1: bottom-right causal mask (qo_len <= kv_len required);
+ *                  0: every row sees all kv_len keys.
+ * workspace        caller-owned device buffer (the wrapper's workspace in the
+ *                  script); the plan writes its metadata (work items, page ids,
+ *                  merge map) to its start with one cudaMemcpyAsync on `stream`
+ *                  and keeps fp32 split-KV partial states after it.  It must stay
+ *                  allocated and untouched while the plan is used.  NULL builds a
+ *                  host-only plan (metadata inspection; run() then fails).
+ * workspace_bytes  its size; PA_ERR_WORKSPACE_TOO_SMALL below the size
+ *                  pagedattn_workspace_size() reports.
+ * opts             NULL or settings (see pagedattn_options).
+ * out_plan         receives the handle; destroy it with pagedattn_plan_destroy.
+ *
+ * Host arrays are read during the call only; the library keeps its own copy.
+ * The call is synchronous on the host and asynchronous on the device (the
+ * metadata copy is queued on `stream`).
+ */
+PAGEDATTN_API pagedattn_status pagedattn_plan(const int32_t* qo_indptr, const int32_t* kv_page_indptr,
+                                const int32_t* kv_page_indices, const int32_t* kv_last_page_len,
+                                int32_t batch_size, int32_t num_qo_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t page_size, int32_t num_pages,
+                                pagedattn_dtype dtype, int32_t causal, void* workspace,
+                                size_t workspace_bytes, const pagedattn_options* opts,
+                                pagedattn_stream_t stream, pagedattn_plan_t* out_plan);
+
+/*
+ * Bytes of workspace the same arguments need (metadata + partial states).
+ * Pure host computation; writes *bytes.
+ */
+PAGEDATTN_API pagedattn_status pagedattn_workspace_size(const int32_t* qo_indptr, const int32_t* kv_page_indptr,
+                                          const int32_t* kv_page_indices,
+                                          const int32_t* kv_last_page_len, int32_t batch_size,
+                                          int32_t num_qo_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t page_size, int32_t num_pages,
+                                          pagedattn_dtype dtype, int32_t causal,
+                                          const pagedattn_options* opts, size_t* bytes);
+
+/*
+ * Attention for the planned batch (the script's forward(q, kv_cache)).
+ *
+ * q        device, dtype[T, Hq, D] contiguous, 16-byte aligned (T = qo_indptr[B]).
+ * kv_cache device, dtype[num_pages, 2, page_size, Hkv, D] contiguous, 16-byte aligned.
+ * out      device, dtype[T, Hq, D], caller-allocated; every row of a request
+ *          with qo_len >= 1 is written.
+ * lse      device, float[T, Hq] natural-log sums, or NULL to skip.
+ * stream   the stream every kernel is queued on.
+ *
+ * Launches the prefill kernel (tcgen05 / TMEM), the decode kernel (CUDA
+ * cores) and, when some request was split, the merge kernel, in that order on
+ * `stream`.  Allocates nothing and does not synchronise the host.  In-kernel
+ * waits are bounded; a wait that gives up sets PA_DEV_TIMEOUT in the device
+ * status word (read it with pagedattn_device_status).  Calls that overlap on
+ * the device must use different workspaces (the partial states live there).
+ */
+PAGEDATTN_API pagedattn_status pagedattn_run(pagedattn_plan_t plan, const void* q, const void* kv_cache,
+                               void* out, float* lse, pagedattn_stream_t stream);
+
+/*
+ * Same as pagedattn_run restricted to the stages in `stage_mask`
+ * (PA_STAGE_* bits).  Running PREFILL, DECODE and MERGE in that order is
+ * exactly pagedattn_run; used to time the kernels one by one.
+ */
+PAGEDATTN_API pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, const void* kv_cache,
+                                      void* out, float* lse, pagedattn_stream_t stream,
+                                      uint32_t stage_mask);
+
+/* Release a plan (end_forward in the script).  NULL is a no-op. */
+PAGEDATTN_API pagedattn_status pagedattn_plan_destroy(pagedattn_plan_t plan);
+
+/* Thread-local text of the last error ("" when none).  Never NULL. */
+PAGEDATTN_API const char* pagedattn_last_error(void);
+
+/*
+ * Wait for `stream`, read the device status word of the plan's workspace
+ * (PA_DEV_* bits OR-ed by the kernels since the plan or the last read) into
+ * *flags and clear it.  Returns PA_ERR_TIMEOUT / PA_ERR_DEVICE_CHECK when a
+ * bit is set, PA_OK otherwise.
+ */
+PAGEDATTN_API pagedattn_status pagedattn_device_status(pagedattn_plan_t plan, pagedattn_stream_t stream,
+                                         int32_t* flags);
+
+/*
+ * Copy the plan metadata (exactly the bytes copied to the workspace) into
+ * host_buf.  With host_buf NULL, only writes the size to *bytes; otherwise
+ * *bytes is the buffer size on input and the bytes written on output.
+ * Layout: int32 words, documented with the planner rules in the source.
+ */
+PAGEDATTN_API pagedattn_status pagedattn_debug_plan_dump(pagedattn_plan_t plan, void* host_buf, size_t* bytes);
+
+/*
+ * Test hook for the page-table walk: a kernel that resolves every logical
+ * token t < kv_len_b of every request b (in request order) with the same
+ * device index code the attention kernels use, writing the physical page id
+ * and slot to page_out / slot_out (device, int32[sum_b kv_len_b]).
+ * Asynchronous on `stream`.
+ */
+PAGEDATTN_API pagedattn_status pagedattn_debug_gather(pagedattn_plan_t plan, int32_t* page_out,
+                                        int32_t* slot_out, pagedattn_stream_t stream);
+
+/* Library version as "major.minor.patch". */
+PAGEDATTN_API const char* pagedattn_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H_ */

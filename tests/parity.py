@@ -1,0 +1,51 @@
+"""Helpers for comparing the CUDA path with the fp64 oracle."""
+import numpy as np
+import torch
+
+import attention_paged_kv_gb300 as pa
+
+LSE_TOL = 1e-3
+
+
+def out_tol(ref: np.ndarray, dtype) -> np.ndarray:
+    """Per-element bound: 2e-3 (fp16) / 1e-2 (bf16), or half an ulp of the
+    output dtype at |ref| plus 1e-3 where that is larger (a bf16 value in
+    [4, 8) already has a half-ulp of 0.0156)."""
+    base = 2e-3 if dtype == torch.float16 else 1e-2
+    mant = 10 if dtype == torch.float16 else 7
+    a = np.maximum(np.abs(ref), 2.0 ** -14)
+    half_ulp = 0.5 * 2.0 ** (np.floor(np.log2(a)) - mant)
+    return np.maximum(base, half_ulp + 1e-3)
+
+
+def run(w, q=None, kv=None, **opts):
+    """Plan + run through the C ABI; returns CPU (out float64, lse float64, plan)."""
+    plan = pa.Plan(**w.plan_args(), dtype=w.dtype, **opts)
+    qd = (w.q if q is None else q).cuda()
+    kvd = (w.kv_cache if kv is None else kv).cuda()
+    out, lse = plan.run(qd, kvd)
+    torch.cuda.synchronize()
+    flags = plan.device_status()
+    assert flags == 0, f"device status {flags}: {pa.last_error()}"
+    return out.to(torch.float64).cpu().numpy(), lse.to(torch.float64).cpu().numpy(), plan
+
+
+def assert_close(out, lse, ref_out, ref_lse, dtype, rows=None, what=""):
+    """Element-wise check of out (tolerance above) and lse (1e-3)."""
+    if rows is not None:
+        out, lse, ref_out, ref_lse = out[rows], lse[rows], ref_out[rows], ref_lse[rows]
+    assert np.isfinite(out).all(), f"{what}: non-finite output"
+    err = np.abs(out - ref_out)
+    tol = out_tol(ref_out, dtype)
+    bad = err > tol
+    allowance = int(((err > (2e-3 if dtype == torch.float16 else 1e-2)) & ~bad).sum())
+    assert not bad.any(), (f"{what}: {int(bad.sum())} outputs off, max err {err.max():.3e} "
+                           f"at {np.unravel_index(err.argmax(), err.shape)}")
+    lerr = np.abs(lse - ref_lse)
+    assert (lerr <= LSE_TOL).all(), f"{what}: lse max err {lerr.max():.3e}"
+    return float(err.max()), float(lerr.max()), allowance
+
+
+def valid_rows(w):
+    """Boolean mask over packed query rows that belong to a request (all rows)."""
+    return np.ones(w.total_qo, bool)

@@ -1,0 +1,222 @@
+"""GPU parity: the CUDA path, called through the C ABI, against the fp64
+oracle on the same seeded inputs, plus the invariants that must hold
+bit-exactly on the GPU (page placement, prefix sharing) and edge cases."""
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import attention as A
+from oracle import plan_ref
+
+pytestmark = pytest.mark.gpu
+
+pa = pytest.importorskip("attention_paged_kv_gb300")
+from parity import assert_close, run  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    pa.load()
+
+
+# ---------------------------------------------------------------- workloads
+
+
+@pytest.mark.parametrize("opts", [{}, {"force_prefill": True}, {"decode_chunk_pages": 1},
+                                  {"prefill_chunk_tiles": 1, "decode_chunk_pages": 1}])
+def test_tiny_all_paths(opts):
+    w = workloads.tiny()
+    ro, rl = A.attention(w, "walk")
+    out, lse, _ = run(w, **opts)
+    assert_close(out, lse, ro, rl, w.dtype, what=f"tiny {opts}")
+
+
+@pytest.mark.parametrize("opts", [{}, {"decode_chunk_pages": 64}, {"decode_chunk_pages": 1}])
+def test_decode_script_batch(opts):
+    w = workloads.decode()
+    ro, rl = A.attention(w)
+    out, lse, plan = run(w, **opts)
+    assert_close(out, lse, ro, rl, w.dtype, what=f"decode {opts}")
+
+
+def test_decode_equals_prefill_qo1():
+    """The timing script's closing check: decode output allclose to the
+    prefill kernel's output on the same qo_len = 1 batch (atol = rtol = 1e-3)."""
+    w = workloads.decode()
+    o_dec, l_dec, _ = run(w)
+    o_pre, l_pre, _ = run(w, force_prefill=True)
+    assert np.allclose(o_dec, o_pre, atol=1e-3, rtol=1e-3)
+    assert np.allclose(l_dec, l_pre, atol=1e-3, rtol=1e-3)
+
+
+def test_ragged_prefill():
+    w = workloads.ragged()
+    ro, rl = A.attention(w)
+    out, lse, _ = run(w)
+    assert_close(out, lse, ro, rl, w.dtype, what="ragged")
+
+
+def test_ragged_padded_equals_unpadded():
+    a = workloads.ragged()
+    b = workloads.ragged(padded=True)
+    oa, la, _ = run(a)
+    ob, lb, _ = run(b)
+    ro, rl = A.attention(a)
+    for r in range(a.batch_size):
+        L = int(a.qo_indptr[r + 1] - a.qo_indptr[r])
+        ra = slice(int(a.qo_indptr[r]), int(a.qo_indptr[r + 1]))
+        rb = slice(200 * r, 200 * r + L)
+        assert_close(ob[rb], lb[rb], ro[ra], rl[ra], a.dtype, what=f"padded request {r}")
+        assert np.allclose(oa[ra], ob[rb], atol=1e-2, rtol=0)
+
+
+def test_ragged_cp_async_equals_tma():
+    w = workloads.ragged()
+    o1, l1, _ = run(w)
+    o2, l2, _ = run(w, force_cp_async=True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_prefix_shared():
+    w = workloads.prefix()
+    ro, rl = A.attention(w)
+    out, lse, _ = run(w)
+    assert_close(out, lse, ro, rl, w.dtype, what="prefix")
+
+
+def test_prefix_shared_equals_duplicated_bitexact():
+    a, b = workloads.prefix(), workloads.prefix(duplicated=True)
+    oa, la, _ = run(a)
+    ob, lb, _ = run(b)
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+@pytest.mark.parametrize("name", ["ragged", "mixed_small", "tiny"])
+def test_page_permutation_bitexact(name):
+    w = workloads.ragged() if name == "ragged" else (
+        workloads.tiny() if name == "tiny" else workloads.mixed(num_decode=24, prefill_len=700, kv_lo=16, kv_hi=3000))
+    o1, l1, _ = run(w)
+    perm = workloads.randperm(w.num_pages, 4242).astype(np.int64)
+    cache2 = torch.empty_like(w.kv_cache)
+    cache2[torch.from_numpy(perm)] = w.kv_cache
+    w.kv_cache = cache2
+    w.kv_page_indices = perm[w.kv_page_indices].astype(np.int32)
+    o2, l2, _ = run(w)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_prefill_split_kv():
+    w = workloads.make_custom("long", [40, 1, 130, 3], [3000, 1500, 2200, 900], 16, 2, 128, 16,
+                              dtype=torch.bfloat16, seed=31)
+    ro, rl = A.attention(w)
+    o1, l1, p1 = run(w, force_prefill=True)
+    o2, l2, p2 = run(w, force_prefill=True, prefill_chunk_tiles=2)
+    h = plan_ref.decode_header(p2.dump())
+    assert h["n_merge"] > 0
+    assert_close(o1, l1, ro, rl, w.dtype, what="unsplit")
+    assert_close(o2, l2, ro, rl, w.dtype, what="split")
+
+
+def test_mixed_step_sampled():
+    """The full mixed batch (8192-token prefill + 256 decodes) on the GPU,
+    checked on sampled rows the oracle computes one by one."""
+    w = workloads.mixed()
+    out, lse, _ = run(w)
+    Hq = w.num_qo_heads
+    pre_tokens = [0, 1, 15, 16, 17, 127, 128, 129, 1000, 2047, 4095, 4096, 6001, 8190, 8191]
+    rows = [(t, h) for t in pre_tokens for h in range(Hq)]
+    dec_reqs = [1, 2, 3, 50, 100, 200, 255, 256]
+    rows += [(int(w.qo_indptr[b]), h) for b in dec_reqs for h in range(Hq)]
+    ref = A.attention_rows(w, rows)
+    ro = np.stack([ref[k][0] for k in rows])
+    rl = np.array([ref[k][1] for k in rows])
+    go = np.stack([out[r, h] for (r, h) in rows])
+    gl = np.array([lse[r, h] for (r, h) in rows])
+    assert_close(go, gl, ro, rl, w.dtype, what="mixed sampled")
+    assert np.isfinite(out).all() and np.isfinite(lse).all()
+
+
+# ---------------------------------------------------------------- indexing / metadata
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "mixed_small"])
+def test_gather_indices_bitexact(name):
+    w = workloads.ragged() if name == "ragged" else (
+        workloads.tiny() if name == "tiny" else workloads.mixed(num_decode=24, prefill_len=700, kv_lo=16, kv_hi=3000))
+    plan = pa.Plan(**w.plan_args(), dtype=w.dtype)
+    pages, slots = plan.debug_gather()
+    torch.cuda.synchronize()
+    rp, rs = A.gather_index_table(w.kv_page_indptr, w.kv_page_indices, w.kv_last_page_len, w.page_size)
+    assert np.array_equal(pages.cpu().numpy(), rp) and np.array_equal(slots.cpu().numpy(), rs)
+
+
+def test_device_metadata_equals_restated_plan():
+    w = workloads.mixed(num_decode=24, prefill_len=700, kv_lo=16, kv_hi=3000)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    plan = pa.Plan(**w.plan_args(), dtype=w.dtype)
+    want = plan_ref.build(**w.plan_args(), dtype=plan_ref.BF16, num_sms=sms)
+    torch.cuda.synchronize()
+    dev = plan.workspace[: want.size * 4].cpu().numpy().view(np.int32)
+    assert np.array_equal(dev, want)
+    assert np.array_equal(plan.dump(), want)
+
+
+# ---------------------------------------------------------------- edge cases
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
+def test_shapes_groups_dtypes(dtype, D, G):
+    Hkv = 2
+    w = workloads.make_custom("s", [1, 7, 1, 33, 0, 140], [1, 7, 300, 200, 5, 333], G * Hkv, Hkv, D, 16,
+                              dtype=dtype, seed=G * 100 + D)
+    ro, rl = A.attention(w)
+    out, lse, _ = run(w)
+    assert_close(out, lse, ro, rl, dtype, what=f"D{D} G{G} {dtype}")
+
+
+@pytest.mark.parametrize("ps", [1, 2, 8, 32, 64, 128])
+def test_page_sizes(ps):
+    w = workloads.make_custom("p", [1, 9, 1, 70], [77, 9, 1, 270], 8, 2, 128, ps, dtype=torch.bfloat16, seed=ps)
+    ro, rl = A.attention(w)
+    out, lse, _ = run(w)
+    assert_close(out, lse, ro, rl, w.dtype, what=f"page_size {ps}")
+
+
+def test_non_causal():
+    w = workloads.make_custom("nc", [3, 1, 150, 20], [2, 7, 40, 300], 8, 4, 64, 8, causal=False,
+                              dtype=torch.float16, seed=77)
+    ro, rl = A.attention(w)
+    out, lse, _ = run(w)
+    assert_close(out, lse, ro, rl, w.dtype, what="non-causal")
+
+
+def test_empty_batch_and_empty_requests():
+    w = workloads.make_custom("e", [], [], 4, 1, 64, 16, seed=7)
+    plan = pa.Plan(**w.plan_args(), dtype=w.dtype)
+    out, lse = plan.run(w.q.cuda(), w.kv_cache.cuda())
+    torch.cuda.synchronize()
+    assert out.numel() == 0
+    w = workloads.make_custom("z", [0, 2, 0, 1], [5, 3, 17, 4], 4, 2, 128, 4, seed=8)
+    ro, rl = A.attention(w)
+    out, lse, _ = run(w)
+    assert_close(out, lse, ro, rl, w.dtype, what="empty requests")
+
+
+def test_single_key_and_constant_v():
+    # row 0 of a qo == kv causal request sees one key: out = V[0] exactly
+    w = workloads.make_custom("k1", [130, 1], [130, 1], 8, 2, 128, 16, dtype=torch.bfloat16, seed=3)
+    out, lse, _ = run(w)
+    for b, r in ((0, 0), (1, 130)):
+        p0 = int(w.kv_page_indices[w.kv_page_indptr[b]])
+        for h in range(8):
+            v0 = w.kv_cache[p0, 1, 0, h // 4].double().numpy()
+            assert np.array_equal(out[r, h], v0)
+    c = torch.randn(128, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    w.kv_cache[:, 1] = c
+    out, lse, _ = run(w)
+    assert np.allclose(out, np.broadcast_to(c.double().numpy(), out.shape), atol=1e-2, rtol=0)

@@ -1,0 +1,197 @@
+"""Host-side tests of the C ABI: the library loads, exports every declared
+symbol, plans bit-for-bit like the restated rules, and rejects bad input
+with the documented status codes.  No GPU is needed."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import plan_ref
+
+pa = pytest.importorskip("attention_paged_kv_gb300")
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(pa.LIB_PATH):
+        from attention_paged_kv_gb300 import build
+        build.build()
+    return pa.load()
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "pagedattn.h")).read()
+    return sorted(set(re.findall(r"PAGEDATTN_API\s+[\w\s\*]+?\b(pagedattn_\w+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol(lib):
+    decl = declared_symbols()
+    assert len(decl) >= 10
+    assert sorted(decl) == sorted(pa.EXPORTED)
+    for name in decl:
+        assert hasattr(lib, name), name
+    assert pa.version() == "0.1.0"
+
+
+def _ref(w, **kw):
+    args = w.plan_args()
+    return plan_ref.build(**args, dtype=plan_ref.FP16 if w.dtype == torch.float16 else plan_ref.BF16, **kw)
+
+
+def _lib_blob(w, **kw):
+    p = pa.Plan(**w.plan_args(), dtype=w.dtype, host_only=True, **kw)
+    try:
+        return p.dump()
+    finally:
+        p.close()
+
+
+CASES = [
+    ("tiny", {}), ("tiny", {"force_prefill": True}), ("tiny", {"prefill_chunk_tiles": 1}),
+    ("decode", {}), ("decode", {"decode_chunk_pages": 3}), ("ragged", {}), ("ragged_padded", {}),
+    ("prefix", {}), ("prefix_dup", {}), ("mixed_small", {}), ("mixed_small", {"prefill_chunk_tiles": 2}),
+    ("random", {}), ("random_nc", {}), ("empty", {}), ("qo0", {}),
+]
+
+
+def make(name):
+    if name == "tiny":
+        return workloads.tiny()
+    if name == "decode":
+        return workloads.decode()
+    if name == "ragged":
+        return workloads.ragged()
+    if name == "ragged_padded":
+        return workloads.ragged(padded=True)
+    if name == "prefix":
+        return workloads.prefix()
+    if name == "prefix_dup":
+        return workloads.prefix(duplicated=True)
+    if name == "mixed_small":
+        return workloads.mixed(num_decode=24, prefill_len=700, kv_lo=16, kv_hi=3000)
+    if name == "random":
+        return workloads.make_custom("r", [1, 5, 0, 130, 1, 64], [9, 300, 4, 130, 2500, 64], 16, 4, 128, 8,
+                                     dtype=torch.bfloat16, seed=5)
+    if name == "random_nc":
+        return workloads.make_custom("r", [3, 1, 200], [2, 7, 40], 8, 8, 64, 2, causal=False, seed=6)
+    if name == "empty":
+        return workloads.make_custom("e", [], [], 4, 1, 64, 16, seed=7)
+    if name == "qo0":
+        return workloads.make_custom("z", [0, 2, 0], [5, 3, 17], 4, 2, 128, 4, seed=8)
+    raise KeyError(name)
+
+
+@pytest.mark.parametrize("name,kw", CASES, ids=[f"{n}-{'-'.join(f'{k}{v}' for k, v in kw.items())}" for n, kw in CASES])
+@pytest.mark.parametrize("sms", [148, 7])
+def test_plan_bit_exact_vs_restated_rules(lib, name, kw, sms):
+    w = make(name)
+    got = _lib_blob(w, num_sms=sms, **kw)
+    want = _ref(w, num_sms=sms, **kw)
+    assert got.shape == want.shape
+    assert np.array_equal(got, want)
+
+
+def test_plan_default_num_sms_needs_device(lib):
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    w = workloads.tiny()
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.Plan(**w.plan_args(), dtype=w.dtype, host_only=True)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+
+
+def _expect(status, w, **over):
+    args = w.plan_args()
+    args.update({k: v for k, v in over.items() if k in args})
+    kw = {k: v for k, v in over.items() if k not in args}
+    kw.setdefault("num_sms", 148)
+    dtype = kw.pop("dtype", w.dtype)
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.Plan(**args, dtype=dtype, host_only=True, **kw)
+    assert e.value.status == status, str(e.value)
+    assert pa.last_error()
+
+
+def test_errors_invalid(lib):
+    w = workloads.tiny()
+    _expect(pa.PA_ERR_INVALID_ARG, w, qo_indptr=np.array([1, 2, 5, 10, 18]))
+    _expect(pa.PA_ERR_INVALID_ARG, w, qo_indptr=np.array([0, 3, 2, 9, 17]))
+    _expect(pa.PA_ERR_INVALID_ARG, w, kv_page_indptr=np.array([0, 2, 1, 11, 17]))
+    # the timing script's literal last page length, seq_length % page_size = 0
+    _expect(pa.PA_ERR_INVALID_ARG, w, kv_last_page_len=np.array([4, 0, 1, 4]))
+    _expect(pa.PA_ERR_INVALID_ARG, w, kv_last_page_len=np.array([4, 5, 1, 4]))
+    bad = w.kv_page_indices.copy()
+    bad[3] = w.num_pages
+    _expect(pa.PA_ERR_INVALID_ARG, w, kv_page_indices=bad)
+    bad[3] = -1
+    _expect(pa.PA_ERR_INVALID_ARG, w, kv_page_indices=bad)
+    _expect(pa.PA_ERR_INVALID_ARG, w, num_qo_heads=3, num_kv_heads=2)
+    # causal: more query rows than keys
+    _expect(pa.PA_ERR_INVALID_ARG, w, qo_indptr=np.array([0, 9, 12, 17, 25]))
+
+
+def test_errors_unsupported(lib):
+    w = workloads.tiny()
+    _expect(pa.PA_ERR_UNSUPPORTED, w, head_dim=96)
+    _expect(pa.PA_ERR_UNSUPPORTED, w, page_size=3)
+    _expect(pa.PA_ERR_UNSUPPORTED, w, page_size=256)
+    _expect(pa.PA_ERR_UNSUPPORTED, w, num_qo_heads=6, num_kv_heads=2)   # group 3 does not divide 128
+    args = w.plan_args()
+    a = [np.ascontiguousarray(np.asarray(args[k], np.int32)) for k in
+         ("qo_indptr", "kv_page_indptr", "kv_page_indices", "kv_last_page_len")]
+    h = ctypes.c_void_p(0)
+    o = pa.Options()
+    o.num_sms = 148
+    P = ctypes.POINTER(ctypes.c_int32)
+    st = lib.pagedattn_plan(*[x.ctypes.data_as(P) for x in a], 4, 2, 1, 64, 4, w.num_pages, 7, 1, None, 0,
+                            ctypes.byref(o), None, ctypes.byref(h))
+    assert st == pa.PA_ERR_UNSUPPORTED
+
+
+def test_workspace_too_small_and_options(lib):
+    w = workloads.tiny()
+    args = w.plan_args()
+    a = [np.ascontiguousarray(np.asarray(args[k], np.int32)) for k in
+         ("qo_indptr", "kv_page_indptr", "kv_page_indices", "kv_last_page_len")]
+    P = ctypes.POINTER(ctypes.c_int32)
+    h = ctypes.c_void_p(0)
+    o = pa.Options()
+    o.num_sms = 148
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: the size check comes first
+    st = lib.pagedattn_plan(*[x.ctypes.data_as(P) for x in a], 4, 2, 1, 64, 4, w.num_pages, 0, 1, fake, 64,
+                            ctypes.byref(o), None, ctypes.byref(h))
+    assert st == pa.PA_ERR_WORKSPACE_TOO_SMALL and not h.value
+    o.reserved[1] = 3
+    st = lib.pagedattn_plan(*[x.ctypes.data_as(P) for x in a], 4, 2, 1, 64, 4, w.num_pages, 0, 1, None, 0,
+                            ctypes.byref(o), None, ctypes.byref(h))
+    assert st == pa.PA_ERR_INVALID_ARG
+    n = pa.workspace_size(**args, dtype=w.dtype, num_sms=148)
+    assert n == plan_ref.decode_header(_ref(w, num_sms=148))["total_bytes"]
+
+
+def test_host_only_plan_cannot_run(lib):
+    w = workloads.tiny()
+    p = pa.Plan(**w.plan_args(), dtype=w.dtype, host_only=True, num_sms=148)
+    st = lib.pagedattn_run(p._h, None, None, None, None, None)
+    assert st == pa.PA_ERR_INVALID_ARG
+    assert lib.pagedattn_plan_destroy(None) == pa.PA_OK
+    p.close()
+
+
+def test_plan_metadata_semantics(lib):
+    """The decode script's batch splits into 4 x 256-key chunks per request
+    on 148 SMs; the mixed batch keeps its long prefill unsplit."""
+    w = workloads.decode()
+    h = plan_ref.decode_header(_lib_blob(w, num_sms=148))
+    assert (h["n_dec"], h["n_pre"], h["n_merge"], h["dec_chunk_pages"]) == (512, 0, 128, 16)
+    w = workloads.mixed(num_decode=8, prefill_len=2048, kv_lo=512, kv_hi=8192)
+    blob = _lib_blob(w, num_sms=148)
+    dec, pre, mer = plan_ref.items(blob)
+    assert (pre[:, 6] == -1).all()                 # no prefill split
+    assert pre[:, 3].max() == 16                   # 16 tokens x 8 heads per tile
+    assert pre[0, 5] - pre[0, 4] == 2048           # longest first
