@@ -29,6 +29,12 @@
 // than 8 in log2 units; p stays below 2^8 in between, which fp32 sums and
 // fp16/bf16 P carry without loss of range.  S_{j+1} is issued before PV_j so
 // the tensor core works while the softmax threads run.
+//
+// Rows that see only a handful of keys average nothing out, so the 8-bit
+// mantissa of a bf16 P would show in their output.  All such rows sit in the
+// first key tile of a sequence; there P is written as hi + lo (two fp16/bf16
+// halves, lo = p - hi) and PV is issued for both, which gives P about 16
+// mantissa bits where it matters for one extra MMA set per item.
 #include "common.cuh"
 #include "internal.h"
 
@@ -52,7 +58,8 @@ struct PreCfg {
   static constexpr int OFF_K = OFF_Q + Q_BYTES;
   static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
   static constexpr int OFF_P = OFF_V + NST * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_P + P_BYTES;
+  static constexpr int OFF_PLO = OFF_P + P_BYTES;    // low half of split P (first key tile)
+  static constexpr int OFF_BAR = OFF_PLO + P_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + alignment slack
 };
 
@@ -89,6 +96,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   const uint32_t sbase = smem_u32(smem);
   const uint32_t q_addr = sbase + C::OFF_Q;
   const uint32_t p_addr = sbase + C::OFF_P;
+  const uint32_t plo_addr = sbase + C::OFF_PLO;
   auto k_addr = [&](int st) { return sbase + C::OFF_K + st * C::KV_BYTES; };
   auto v_addr = [&](int st) { return sbase + C::OFF_V + st * C::KV_BYTES; };
 
@@ -108,6 +116,9 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   const PreItem it = p.pre[blockIdx.x];
   const ReqEntry rq = p.req[it.req];
   const int nkt = (it.kv_tok1 - it.kv_tok0 + kKvTile - 1) / kKvTile;
+  // split P on the first key tile when some row of the item sees < 128 keys
+  const int first_vis = p.causal ? (rq.kv_len - rq.qo_len + it.q_tok0 + 1) : rq.kv_len;
+  const bool lo_split0 = (it.kv_tok0 == 0) && (first_vis < kKvTile);
 
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
@@ -240,6 +251,14 @@ __global__ void __launch_bounds__(kPreThreads, 1)
             tc_mma_ss(tmem + kColO, smem_desc_sw128(p_addr + aoff, 16, 1024),
                       smem_desc_sw128(v_addr(st) + k * 2048, C::BLK, 1024), id_o, (i > 0 || k > 0) ? 1u : 0u);
           }
+          if (i == 0 && lo_split0) {
+#pragma unroll
+            for (int k = 0; k < kKvTile / 16; ++k) {
+              const uint32_t aoff = (k >> 2) * C::BLK + (k & 3) * 32;
+              tc_mma_ss(tmem + kColO, smem_desc_sw128(plo_addr + aoff, 16, 1024),
+                        smem_desc_sw128(v_addr(st) + k * 2048, C::BLK, 1024), id_o, 1u);
+            }
+          }
           tc_commit(&empty[st]);
           tc_commit(o_done);
         }
@@ -295,9 +314,12 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       tmem_wait_ld();
 #pragma unroll
       for (int i = 0; i < 128; ++i) asm volatile("" : "+r"(s[i]));
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[j & 1]);
+      const bool lo_split = lo_split0 && j == 0;
+      if (!lo_split) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[j & 1]);
+      }
 
       // mask (diagonal / tail tiles only) and tile max
       const int lim = row_end - k0;
@@ -380,6 +402,38 @@ __global__ void __launch_bounds__(kPreThreads, 1)
                                pw[kb * 32 + c * 4 + 3]);
           *reinterpret_cast<uint4*>(smem + C::OFF_P + kb * C::BLK + r * 128 + ((c ^ (r & 7)) * 16)) = v;
         }
+      if (lo_split) {
+        // second pass over S (still in TMEM: its buffer is only released
+        // below): the same p values again, minus their rounded high halves
+        tmem_ld32(sa + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
+        tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+        tmem_ld32(sa + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
+        tmem_ld32(sa + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
+        tmem_wait_ld();
+#pragma unroll
+        for (int i = 0; i < 128; ++i) asm volatile("" : "+r"(s[i]));
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&s_free[j & 1]);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint32_t lw[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int col = kb * 64 + c * 8 + 2 * u;
+              const float va = (col < lim) ? __uint_as_float(s[col]) : -INFINITY;
+              const float vb = (col + 1 < lim) ? __uint_as_float(s[col + 1]) : -INFINITY;
+              const float a = ex2(fmaf(va, sl2, -m_use));
+              const float b = ex2(fmaf(vb, sl2, -m_use));
+              const float2 hi = Elt<T>::to_f2(Elt<T>::from_f2(a, b));
+              lw[u] = Elt<T>::from_f2(a - hi.x, b - hi.y);
+            }
+            *reinterpret_cast<uint4*>(smem + C::OFF_PLO + kb * C::BLK + r * 128 + ((c ^ (r & 7)) * 16)) =
+                make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+      }
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
