@@ -43,7 +43,8 @@ DEFAULT_WORKSPACE_BYTES = 128 * 1024 * 1024  # the timing script's workspace siz
 # every symbol include/pagedattn.h declares
 EXPORTED = ("pagedattn_plan", "pagedattn_workspace_size", "pagedattn_run", "pagedattn_run_stages",
             "pagedattn_plan_destroy", "pagedattn_last_error", "pagedattn_device_status",
-            "pagedattn_debug_plan_dump", "pagedattn_debug_gather", "pagedattn_version")
+            "pagedattn_debug_plan_dump", "pagedattn_debug_gather", "pagedattn_version",
+            "pagedattn_run_decode_noalloc")
 
 
 class PagedAttnError(RuntimeError):
@@ -94,6 +95,8 @@ def load() -> ctypes.CDLL:
         lib.pagedattn_debug_plan_dump.restype = ctypes.c_int
         lib.pagedattn_debug_gather.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p]
         lib.pagedattn_debug_gather.restype = ctypes.c_int
+        lib.pagedattn_run_decode_noalloc.argtypes = [ctypes.c_void_p] * 6
+        lib.pagedattn_run_decode_noalloc.restype = ctypes.c_int
         lib.pagedattn_version.argtypes = []
         lib.pagedattn_version.restype = ctypes.c_char_p
         _lib = lib

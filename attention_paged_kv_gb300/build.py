@@ -18,7 +18,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpagedattn.so")
-SOURCES = ["api.cu", "plan.cpp", "prefill.cu", "decode.cu"]
+SOURCES = ["api.cu", "plan.cpp", "prefill.cu", "decode.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -12,21 +12,13 @@
 #include "common.cuh"
 #include "internal.h"
 
-struct pagedattn_plan_s {
-  pa::HostPlan hp;
-  void* workspace = nullptr;
-  size_t workspace_bytes = 0;
-  int device = -1;
-  int force_cp_async = 0;
-  // tensor maps over the last kv_cache pointer seen by run()
-  const void* map_kv = nullptr;
-  CUtensorMap map_rows;   // decode: box {D, 1, min(ps, 64), 1}, no swizzle
-  CUtensorMap map_sw128;  // prefill: box {64, 1, ps, 1}, 128-byte swizzle
-};
-
 namespace {
 
 thread_local std::string g_last_error;
+
+}  // namespace
+
+namespace pa {
 
 pagedattn_status set_err(pagedattn_status s, const std::string& msg) {
   g_last_error = msg;
@@ -36,6 +28,13 @@ pagedattn_status set_err(pagedattn_status s, const std::string& msg) {
 pagedattn_status cuda_err(cudaError_t e, const char* what) {
   return set_err(PA_ERR_CUDA, std::string(what) + ": " + cudaGetErrorName(e) + " (" + cudaGetErrorString(e) + ")");
 }
+
+}  // namespace pa
+
+using pa::cuda_err;
+using pa::set_err;
+
+namespace {
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -55,6 +54,10 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+}  // namespace
+
+namespace pa {
+
 // 4-D view of the cache: (D, Hkv, page_size, 2 * num_pages), innermost first.
 pagedattn_status encode_kv_map(CUtensorMap* m, const pa::HostPlan& hp, const void* kv, uint32_t box0,
                                uint32_t box2, CUtensorMapSwizzle sw) {
@@ -72,6 +75,12 @@ pagedattn_status encode_kv_map(CUtensorMap* m, const pa::HostPlan& hp, const voi
   if (r != CUDA_SUCCESS) return set_err(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed, code " + std::to_string(int(r)));
   return PA_OK;
 }
+
+}  // namespace pa
+
+using pa::encode_kv_map;
+
+namespace {
 
 pagedattn_status fill_inputs(pa::PlanInputs* in, const int32_t* qo_indptr, const int32_t* kv_page_indptr,
                              const int32_t* kv_page_indices, const int32_t* kv_last_page_len, int32_t batch_size,

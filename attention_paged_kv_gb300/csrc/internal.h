@@ -53,4 +53,26 @@ cudaError_t launch_decode(const RunArgs& a, const CUtensorMap* map_rows);
 cudaError_t launch_merge(const RunArgs& a);
 cudaError_t launch_debug_gather(const RunArgs& a, int32_t* page_out, int32_t* slot_out);
 
+// Error reporting into the thread-local last-error text (api.cu).
+pagedattn_status set_err(pagedattn_status s, const std::string& msg);
+pagedattn_status cuda_err(cudaError_t e, const char* what);
+
+// Tensor map over the cache viewed as (D, Hkv, page_size, 2 * num_pages),
+// box {box0, 1, box2, 1} (api.cu).
+pagedattn_status encode_kv_map(CUtensorMap* m, const HostPlan& hp, const void* kv, uint32_t box0, uint32_t box2,
+                               CUtensorMapSwizzle sw);
+
 }  // namespace pa
+
+// The plan handle behind pagedattn_plan_t.
+struct pagedattn_plan_s {
+  pa::HostPlan hp;
+  void* workspace = nullptr;
+  size_t workspace_bytes = 0;
+  int device = -1;
+  int force_cp_async = 0;
+  // tensor maps over the last kv_cache pointer seen by run()
+  const void* map_kv = nullptr;
+  CUtensorMap map_rows;   // decode: box {D, 1, min(ps, 64), 1}, no swizzle
+  CUtensorMap map_sw128;  // prefill: box {64, 1, ps, 1}, 128-byte swizzle
+};

@@ -205,6 +205,37 @@ PAGEDATTN_API pagedattn_status pagedattn_debug_plan_dump(pagedattn_plan_t plan, 
 PAGEDATTN_API pagedattn_status pagedattn_debug_gather(pagedattn_plan_t plan, int32_t* page_out,
                                         int32_t* slot_out, pagedattn_stream_t stream);
 
+/*
+ * Decode without a device workspace.  The source pages have no counterpart
+ * to this call; it exists for callers that cannot allocate device memory --
+ * serving processes that reserve all free GPU memory for their KV cache up
+ * front, and latency-critical code that must not call cudaFree (which
+ * synchronises the device).
+ *
+ * Runs the decode kernel and the split merge of `plan` (build it with
+ * pagedattn_plan and workspace = NULL) with the plan's metadata and split-KV
+ * partial states in a fixed 16 MiB device array inside the library instead
+ * of a caller workspace.  The array exists once per GPU that loads the
+ * library and stays allocated until the process exits.  q, kv_cache, out and
+ * lse are as for pagedattn_run.
+ *
+ * The batch must be decode-only (every request has qo_len 0 or 1, the group
+ * size num_qo_heads / num_kv_heads is 1, 2, 4 or 8, and force_prefill is
+ * off): PA_ERR_UNSUPPORTED otherwise.  A plan whose metadata and partial
+ * states exceed 16 MiB returns PA_ERR_WORKSPACE_TOO_SMALL (plan with a larger
+ * decode_chunk_pages).  The call allocates no memory.  Its first call on a
+ * device looks up the array's device address (cudaGetSymbolAddress) while
+ * that device is current; make that first call before any stream capture.
+ * Every call overwrites the array, whose contents are whatever the last call
+ * left (the plan's metadata copy clears the in-kernel status word): calls
+ * that overlap on the GPU -- on different streams or from different host
+ * threads -- race and must not be issued.  The in-kernel status word of this
+ * variant is not reported.
+ */
+PAGEDATTN_API pagedattn_status pagedattn_run_decode_noalloc(pagedattn_plan_t plan, const void* q,
+                                                            const void* kv_cache, void* out, float* lse,
+                                                            pagedattn_stream_t stream);
+
 /* Library version as "major.minor.patch". */
 PAGEDATTN_API const char* pagedattn_version(void);
 
