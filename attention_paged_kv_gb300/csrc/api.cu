@@ -252,10 +252,10 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
   if (dev != plan->device) return set_err(PA_ERR_INVALID_ARG, "current device differs from the plan's device");
 
   if ((hp.n_pre > 0 || hp.n_dec > 0) && kv_cache != plan->map_kv) {
-    pagedattn_status s = encode_kv_map(&plan->map_rows, hp, kv_cache, uint32_t(hp.D),
-                                       uint32_t(hp.ps < 64 ? hp.ps : 64), CU_TENSOR_MAP_SWIZZLE_NONE);
-    if (s != PA_OK) return s;
     if (hp.ps >= 8) {
+      pagedattn_status s = encode_kv_map(&plan->map_rows, hp, kv_cache, 64, uint32_t(hp.ps < 64 ? hp.ps : 64),
+                                         CU_TENSOR_MAP_SWIZZLE_128B);
+      if (s != PA_OK) return s;
       s = encode_kv_map(&plan->map_sw128, hp, kv_cache, 64, uint32_t(hp.ps), CU_TENSOR_MAP_SWIZZLE_128B);
       if (s != PA_OK) return s;
     }
@@ -275,7 +275,7 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
     if (e != cudaSuccess) return cuda_err(e, "prefill launch");
   }
   if (stage_mask & PA_STAGE_DECODE) {
-    e = pa::launch_decode(a, &plan->map_rows);
+    e = pa::launch_decode(a, hp.ps >= 8 ? &plan->map_rows : nullptr);
     if (e != cudaSuccess) return cuda_err(e, "decode launch");
   }
   if (stage_mask & PA_STAGE_MERGE) {

@@ -7,17 +7,26 @@
 // request when the planner cut it for kv-parallelism (the issue's split-k);
 // a split then writes an fp32 partial state that the merge kernel combines.
 //
-//   warp 4     producer: TMA copies of whole page rows ([slots, D] of one kv
-//              head) through the page table, 64 keys per stage, 3 stages.
-//   warps 0-3  each takes 16 of the stage's 64 keys.  A key is read by D/8
-//              lanes, 16 bytes each (coalesced rows out of shared memory);
-//              every lane holds its 8 columns of q for all G query heads of
-//              the group in registers, so each K/V element loaded serves G
-//              heads.  Partial dot products are reduce-scattered over the
-//              lanes of a key (one shuffle round per halving of the head
-//              count), scores go through a small per-warp buffer for the
-//              online softmax, and O accumulates in registers.
-// At the end the four warps' (max, sum, O) states are combined in shared memory.
+//   warp 4     producer: TMA copies of page rows ([slots, 64 columns] boxes,
+//              128-byte swizzle) through the page table, 64 keys per stage,
+//              3 stages; pages of fewer than 8 slots go through cp.async with
+//              the same swizzle.
+//   warps 0..P-1   QK + softmax for P (QK, PV) pairs; warp i takes stages
+//              i, i+P, i+2P, ...
+//              Each lane owns two keys of the stage and computes their dot
+//              products with all G query heads; q (pre-scaled, fp32 column
+//              pairs) is read from shared memory by broadcast, K rows through
+//              the swizzle without bank conflicts, and no shuffles are needed
+//              until the per-head max and sum of the stage.  The warp keeps
+//              the running max / sum per head and hands P (and the factor that
+//              rescales O) to its PV partner through shared memory.
+//   warps P..2P-1  PV: warp P+i accumulates O for warp i's stages; a key's V row
+//              is read by D/8 lanes, 16 bytes each, and every lane holds its 8
+//              columns of O for all G heads, so one load of a V element feeds
+//              G heads.
+// The producer is warp 2P.  All products are packed f32x2 FMAs on two
+// adjacent head-dim columns.  The pairs keep separate softmax states,
+// combined at the end.
 #include <cstring>
 
 #include "common.cuh"
@@ -26,8 +35,15 @@
 namespace pa {
 namespace {
 
-constexpr int kDecThreads = 160;
-constexpr int kDecStages = 3;
+#ifndef PA_DEC_PAIRS
+#define PA_DEC_PAIRS 2
+#endif
+constexpr int kDecPairs = PA_DEC_PAIRS;           // (QK, PV) warp pairs per CTA
+constexpr int kDecThreads = 32 * (2 * kDecPairs + 1);  // + 1 producer warp
+#ifndef PA_DEC_STAGES
+#define PA_DEC_STAGES 3
+#endif
+constexpr int kDecStages = PA_DEC_STAGES;
 constexpr int kDecTile = 64;  // keys per stage
 constexpr float kLn2f = 0.6931471805599453f;
 constexpr float kLog2e = 1.4426950408889634f;
@@ -40,74 +56,75 @@ __device__ __forceinline__ float ex2f(float x) {
 
 template <int D>
 struct DecCfg {
-  static constexpr int ROW = D * 2;                   // bytes of one K or V row
-  static constexpr int STAGE_K = kDecTile * ROW;
+  static constexpr int NKB = D / 64;                  // 128-byte column blocks of a row
+  static constexpr int BLK = kDecTile * 128;          // 64 rows x 128 bytes
+  static constexpr int STAGE_K = NKB * BLK;
   static constexpr int STAGE = 2 * STAGE_K;           // K then V
-  static constexpr int OFF_S = kDecStages * STAGE;    // per-warp score buffers
-  static constexpr int S_BYTES = 4 * 16 * 8 * 4;      // 4 warps x 16 keys x up to 8 heads
-  static constexpr int OFF_BAR = OFF_S + S_BYTES;
-  static constexpr int SMEM = OFF_BAR + 128 + 128;
+  static constexpr int OFF_Q = kDecStages * STAGE;    // q: up to 8 heads x D fp32
+  static constexpr int OFF_P = OFF_Q + 8 * D * 4;     // P as (p, p) pairs: per pair 64 keys x 8 heads
+  static constexpr int OFF_A = OFF_P + kDecPairs * kDecTile * 8 * 8;  // O rescale factor per (pair, head)
+  static constexpr int OFF_BAR = OFF_A + kDecPairs * 8 * 4;
+  static constexpr int BAR_BYTES = (2 * kDecStages + 2 * kDecPairs) * 8 + 8;  // + abort flag
+  static constexpr int SMEM = OFF_BAR + ((BAR_BYTES + 127) / 128) * 128 + 1024;  // + alignment slack
 };
 
-template <int N>
-struct Log2 { static constexpr int v = 1 + Log2<N / 2>::v; };
-template <>
-struct Log2<1> { static constexpr int v = 0; };
-
-// Reduce-scatter G per-lane partial sums across the LPT lanes of one key:
-// afterwards every lane holds the full sum for head (lane % LPT) / (LPT / G).
-template <int G, int LPT>
-__device__ __forceinline__ float reduce_scatter(float (&v)[G], int lane) {
-  static_assert(G <= LPT, "group larger than lanes per key");
-#pragma unroll
-  for (int n = G / 2, off = LPT / 2; n >= 1; n /= 2, off /= 2) {
-    const bool upper = (lane & off) != 0;
-#pragma unroll
-    for (int k = 0; k < n; ++k) {
-      const float send = upper ? v[k] : v[k + n];
-      const float keep = upper ? v[k + n] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xffffffffu, send, off);
-    }
-  }
-  float r = v[0];
-#pragma unroll
-  for (int off = LPT / (2 * G); off >= 1; off /= 2) r += __shfl_xor_sync(0xffffffffu, r, off);
-  return r;
+// Byte offset of 16-byte chunk c (of the row's D/8) of key row t in a stage
+// half (K or V) laid out by the 128-byte swizzle: column blocks of 64
+// elements, 128-byte rows, chunk index XOR (row mod 8).
+template <int D>
+__device__ __forceinline__ uint32_t sw_off(int t, int c) {
+  return static_cast<uint32_t>((c >> 3) * DecCfg<D>::BLK + t * 128 + (((c & 7) ^ (t & 7)) << 4));
 }
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kDecThreads, 2)
-    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p) {
+__global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p,
+                                               const int use_tma) {
   using C = DecCfg<D>;
-  constexpr int LPT = D / 8;       // lanes per key
-  constexpr int TPW = 32 / LPT;    // keys per warp step
-  constexpr int STEPS = 16 / TPW;  // steps per warp per stage
-  constexpr int VPL = (16 * G >= 32) ? (16 * G) / 32 : 1;
-  extern __shared__ __align__(128) uint8_t smem[];
+  constexpr int NKB = C::NKB;
+  constexpr int NCH = D / 8;       // 16-byte chunks per row
+  constexpr int LPT = D / 8;       // PV lanes per key
+  constexpr int TPS = 32 / LPT;    // PV keys per warp step
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + kDecStages;
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(empty + kDecStages);
+  uint64_t* pfull = empty + kDecStages;  // [pairs] QK -> PV
+  uint64_t* pempty = pfull + kDecPairs;  // [pairs] PV -> QK
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(pempty + kDecPairs);
+  float2* qs2 = reinterpret_cast<float2*>(smem + C::OFF_Q);  // [G][D/2]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const DecItem it = p.dec[blockIdx.x];
   const ReqEntry rq = p.req[it.req];
   const int nstage = (it.tok1 - it.tok0 + kDecTile - 1) / kDecTile;
+  const int64_t qrow0 = int64_t(rq.qo_start) * p.Hq + int64_t(it.kv_head) * G;
 
   if (tid == 0) {
     for (int i = 0; i < kDecStages; ++i) {
-      mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 4);
+      mbar_init(&full[i], use_tma ? 1 : 32);
+      mbar_init(&empty[i], 2);
+    }
+    for (int i = 0; i < kDecPairs; ++i) {
+      mbar_init(&pfull[i], 1);
+      mbar_init(&pempty[i], 1);
     }
     *abort_flag = 0;
     mbar_init_fence();
   }
+  // q for the G heads, pre-scaled into log2 units, as fp32 column pairs
+  for (int idx = tid; idx < G * D / 2; idx += kDecThreads) {
+    const int g = idx / (D / 2), c2 = idx % (D / 2);
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) + (qrow0 + g) * D) + c2);
+    qs2[idx] = __fmul2_rn(Elt<T>::to_f2(w), make_float2(p.scale_log2, p.scale_log2));
+  }
   __syncthreads();
 
-  if (warp == 4) {
+  if (warp == 2 * kDecPairs) {
     // ---------------------------------------------------------------- producer
-    if (lane == 0) tma_prefetch_desc(&kv_map);
+    if (use_tma && lane == 0) tma_prefetch_desc(&kv_map);
     const int br_shift = min(p.ps_shift, 6);
     const int BR = 1 << br_shift;  // rows per copy: a page, or 64 slots of it
+    const uint32_t sbase = smem_u32(smem);
     int issued = 0;
     for (int j = 0; j < nstage; ++j) {
       const int st = j % kDecStages;
@@ -119,23 +136,56 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       }
       const int s0 = it.tok0 + j * kDecTile;
       const int s1 = min(s0 + kDecTile, it.tok1);
-      const int nbox = (s1 - s0 + BR - 1) >> br_shift;
-      if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(nbox * BR * C::ROW * 2));
-      __syncwarp();
-      const uint32_t kdst = smem_u32(smem) + st * C::STAGE;
-      for (int b = lane; b < nbox; b += 32) {
-        const KvLoc loc = kv_locate(p.pages, rq.page_start, s0 + b * BR, p.ps_shift);
-        int pid = loc.page;
-        if (static_cast<unsigned>(pid) >= static_cast<unsigned>(p.num_pages)) {
-          atomicOr(p.status, PA_DEV_BAD_INDEX);
-          pid = 0;
+      const uint32_t kdst = sbase + st * C::STAGE;
+      if (use_tma) {
+        const int nbox = (s1 - s0 + BR - 1) >> br_shift;
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(nbox * BR * 128 * NKB * 2));
+        __syncwarp();
+        for (int b = lane; b < nbox; b += 32) {
+          const KvLoc loc = kv_locate(p.pages, rq.page_start, s0 + b * BR, p.ps_shift);
+          int pid = loc.page;
+          if (static_cast<unsigned>(pid) >= static_cast<unsigned>(p.num_pages)) {
+            atomicOr(p.status, PA_DEV_BAD_INDEX);
+            pid = 0;
+          }
+#pragma unroll
+          for (int kb = 0; kb < NKB; ++kb) {
+            tma_load_4d(kdst + kb * C::BLK + b * BR * 128, &kv_map, kb * 64, it.kv_head, loc.slot, 2 * pid,
+                        &full[st]);
+            tma_load_4d(kdst + C::STAGE_K + kb * C::BLK + b * BR * 128, &kv_map, kb * 64, it.kv_head, loc.slot,
+                        2 * pid + 1, &full[st]);
+          }
         }
-        tma_load_4d(kdst + b * BR * C::ROW, &kv_map, 0, it.kv_head, loc.slot, 2 * pid, &full[st]);
-        tma_load_4d(kdst + C::STAGE_K + b * BR * C::ROW, &kv_map, 0, it.kv_head, loc.slot, 2 * pid + 1, &full[st]);
+      } else {
+        const T* kvb = static_cast<const T*>(p.kv);
+        for (int t = lane; t < kDecTile; t += 32) {
+          const bool valid = s0 + t < s1;
+          const T* srck = kvb;
+          const T* srcv = kvb;
+          if (valid) {
+            const KvLoc loc = kv_locate(p.pages, rq.page_start, s0 + t, p.ps_shift);
+            int pid = loc.page;
+            if (static_cast<unsigned>(pid) >= static_cast<unsigned>(p.num_pages)) {
+              atomicOr(p.status, PA_DEV_BAD_INDEX);
+              pid = 0;
+            }
+            const size_t rowk = ((size_t(pid) * 2 * p.ps + loc.slot) * p.Hkv + it.kv_head) * D;
+            srck = kvb + rowk;
+            srcv = kvb + rowk + size_t(p.ps) * p.Hkv * D;
+          }
+#pragma unroll
+          for (int c = 0; c < NCH; ++c) {
+            cp_async16(kdst + sw_off<D>(t, c), srck + (valid ? c * 8 : 0), valid ? 16u : 0u);
+            cp_async16(kdst + C::STAGE_K + sw_off<D>(t, c), srcv + (valid ? c * 8 : 0), valid ? 16u : 0u);
+          }
+        }
+        cp_async_commit();
+        cp_async_wait_all();
+        mbar_arrive(&full[st]);
       }
       issued = j + 1;
     }
-    if (lane == 0) {
+    if (use_tma && lane == 0) {
       for (int j = max(0, issued - kDecStages); j < issued; ++j) {
         const uint32_t a = smem_u32(&full[j % kDecStages]);
         const long long t0 = clock64();
@@ -144,175 +194,191 @@ __global__ void __launch_bounds__(kDecThreads, 2)
       }
     }
     __syncwarp();
-    asm volatile("bar.arrive 1, 160;" ::: "memory");
+    asm volatile("bar.arrive 1, %0;" ::"n"(kDecThreads) : "memory");
     return;
   }
 
-  // ---------------------------------------------------------------- compute warps
-  const int tg = lane / LPT;   // key slot within a warp step
-  const int ds = lane % LPT;   // 8-column slice
-  const int hsel = ds / (LPT / G);
-  const bool writer = (ds % (LPT / G)) == 0;
-  const int64_t qrow0 = int64_t(rq.qo_start) * p.Hq + int64_t(it.kv_head) * G;
+  const int pair = warp % kDecPairs;
+  float2* pbuf = reinterpret_cast<float2*>(smem + C::OFF_P) + pair * kDecTile * 8;  // [64 keys][8 heads]
+  float* abuf = reinterpret_cast<float*>(smem + C::OFF_A) + pair * 8;
+  float* comb_o = reinterpret_cast<float*>(smem);  // [pairs][G][D], reuses stage memory at the end
+  float* comb_m = comb_o + kDecPairs * G * D;      // [pairs][G]
+  float* comb_l = comb_m + kDecPairs * G;          // [pairs][G]
 
-  float qf[G][8];
-#pragma unroll
-  for (int g = 0; g < G; ++g) {
-    const uint4 raw = __ldg(reinterpret_cast<const uint4*>(static_cast<const T*>(p.q) + (qrow0 + g) * D + ds * 8));
-    const uint32_t w4[4] = {raw.x, raw.y, raw.z, raw.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = Elt<T>::to_f2(w4[i]);
-      qf[g][2 * i] = f.x * p.scale_log2;
-      qf[g][2 * i + 1] = f.y * p.scale_log2;
-    }
-  }
-  float o[G][8];
-#pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int i = 0; i < 8; ++i) o[g][i] = 0.f;
-  float m_run = -INFINITY, l_run = 0.f;  // state of head (lane % G)
-  float* sw = reinterpret_cast<float*>(smem + C::OFF_S) + warp * 16 * G;
-  const int hl = lane % G;
-
-  for (int j = 0; j < nstage; ++j) {
-    const int st = j % kDecStages;
-    bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status);
-    if (!__all_sync(0xffffffffu, ok)) break;
-    const int s0 = it.tok0 + j * kDecTile;
-    const int nval = min(kDecTile, it.tok1 - s0);
-    const int wt0 = warp * 16;
-    const int wval = max(0, min(16, nval - wt0));
-    const uint8_t* kst = smem + st * C::STAGE;
-    const uint8_t* vst = kst + C::STAGE_K;
-
-    // scores for this warp's 16 keys
-#pragma unroll
-    for (int stp = 0; stp < STEPS; ++stp) {
-      const int t = stp * TPW + tg;
-      const uint4 kraw = *reinterpret_cast<const uint4*>(kst + (wt0 + t) * C::ROW + ds * 16);
-      const uint32_t w4[4] = {kraw.x, kraw.y, kraw.z, kraw.w};
-      float kf[8];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = Elt<T>::to_f2(w4[i]);
-        kf[2 * i] = f.x;
-        kf[2 * i + 1] = f.y;
-      }
-      float acc[G];
-#pragma unroll
-      for (int g = 0; g < G; ++g) {
-        float a = 0.f;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) a = fmaf(qf[g][i], kf[i], a);
-        acc[g] = a;
-      }
-      const float s = reduce_scatter<G, LPT>(acc, lane);
-      if (writer) sw[t * G + hsel] = (t < wval) ? s : -INFINITY;
-    }
-    __syncwarp();
-
-    // online softmax over the 16 keys, lane owns head hl
-    float sv[VPL];
-    float mx = -INFINITY;
-#pragma unroll
-    for (int k = 0; k < VPL; ++k) {
-      const int tt = lane / G + k * (32 / G);
-      sv[k] = (tt < 16) ? sw[tt * G + hl] : -INFINITY;
-      mx = fmaxf(mx, sv[k]);
-    }
-#pragma unroll
-    for (int off = G; off < 32; off *= 2) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-    const float m_new = fmaxf(m_run, mx);
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    const float alpha = ex2f(m_run - m_use);
-    float psum = 0.f;
-#pragma unroll
-    for (int k = 0; k < VPL; ++k) {
-      const int tt = lane / G + k * (32 / G);
-      const float pv = ex2f(sv[k] - m_use);
-      if (tt < 16) sw[tt * G + hl] = pv;
-      psum += (tt < 16) ? pv : 0.f;
-    }
-#pragma unroll
-    for (int off = G; off < 32; off *= 2) psum += __shfl_xor_sync(0xffffffffu, psum, off);
-    l_run = l_run * alpha + psum;
-    m_run = m_new;
+  if (warp < kDecPairs) {
+    // ---------------------------------------------------------------- QK + softmax
+    float m_run[G], l_run[G];
 #pragma unroll
     for (int g = 0; g < G; ++g) {
-      const float ag = __shfl_sync(0xffffffffu, alpha, g);
-#pragma unroll
-      for (int i = 0; i < 8; ++i) o[g][i] *= ag;
+      m_run[g] = -INFINITY;
+      l_run[g] = 0.f;
     }
-    __syncwarp();
-
-    // O += P V over the warp's valid keys
+    const int t0 = lane, t1 = lane + 32;
+    for (int k = 0, j = pair; j < nstage; ++k, j += kDecPairs) {
+      const int st = j % kDecStages;
+      bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int nval = min(kDecTile, it.tok1 - (it.tok0 + j * kDecTile));
+      const uint8_t* kst = smem + st * C::STAGE;
+      float2 a0[G], a1[G];
 #pragma unroll
-    for (int stp = 0; stp < STEPS; ++stp) {
-      const int t = stp * TPW + tg;
-      if (t < wval) {
-        const uint4 vraw = *reinterpret_cast<const uint4*>(vst + (wt0 + t) * C::ROW + ds * 16);
-        const uint32_t w4[4] = {vraw.x, vraw.y, vraw.z, vraw.w};
-        float vf[8];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = Elt<T>::to_f2(w4[i]);
-          vf[2 * i] = f.x;
-          vf[2 * i + 1] = f.y;
-        }
+      for (int g = 0; g < G; ++g) {
+        a0[g] = make_float2(0.f, 0.f);
+        a1[g] = make_float2(0.f, 0.f);
+      }
+#pragma unroll 4
+      for (int c = 0; c < NCH; ++c) {
+        const uint4 r0 = *reinterpret_cast<const uint4*>(kst + sw_off<D>(t0, c));
+        const uint4 r1 = *reinterpret_cast<const uint4*>(kst + sw_off<D>(t1, c));
+        const float2 k0[4] = {Elt<T>::to_f2(r0.x), Elt<T>::to_f2(r0.y), Elt<T>::to_f2(r0.z), Elt<T>::to_f2(r0.w)};
+        const float2 k1[4] = {Elt<T>::to_f2(r1.x), Elt<T>::to_f2(r1.y), Elt<T>::to_f2(r1.z), Elt<T>::to_f2(r1.w)};
 #pragma unroll
         for (int g = 0; g < G; ++g) {
-          const float pg = sw[t * G + g];
+          const float4 qa = *reinterpret_cast<const float4*>(qs2 + g * (D / 2) + c * 4);
+          const float4 qb = *reinterpret_cast<const float4*>(qs2 + g * (D / 2) + c * 4 + 2);
+          const float2 q4[4] = {make_float2(qa.x, qa.y), make_float2(qa.z, qa.w), make_float2(qb.x, qb.y),
+                                make_float2(qb.z, qb.w)};
 #pragma unroll
-          for (int i = 0; i < 8; ++i) o[g][i] = fmaf(pg, vf[i], o[g][i]);
+          for (int i = 0; i < 4; ++i) {
+            a0[g] = __ffma2_rn(q4[i], k0[i], a0[g]);
+            a1[g] = __ffma2_rn(q4[i], k1[i], a1[g]);
+          }
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);  // this warp is done with K of the stage
+
+      float alpha[G], p0[G], p1[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        const float s0 = (t0 < nval) ? a0[g].x + a0[g].y : -INFINITY;
+        const float s1 = (t1 < nval) ? a1[g].x + a1[g].y : -INFINITY;
+        float mx = fmaxf(s0, s1);
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+        const float m_new = fmaxf(m_run[g], mx);
+        const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+        alpha[g] = ex2f(m_run[g] - m_use);
+        p0[g] = ex2f(s0 - m_use);
+        p1[g] = ex2f(s1 - m_use);
+        float sum = p0[g] + p1[g];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+        l_run[g] = l_run[g] * alpha[g] + sum;
+        m_run[g] = m_new;
+      }
+      if (k >= 1) {
+        ok = mbar_wait(&pempty[pair], (k - 1) & 1, abort_flag, p.status);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        pbuf[t0 * 8 + g] = make_float2(p0[g], p0[g]);
+        pbuf[t1 * 8 + g] = make_float2(p1[g], p1[g]);
+      }
+      if (lane == 0) {
+#pragma unroll
+        for (int g = 0; g < G; ++g) abuf[g] = alpha[g];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&pfull[pair]);
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-  }
-
-  // ---------------------------------------------------------------- combine
-  // sum O over the TPW key slots of the warp
+    asm volatile("bar.sync 1, %0;" ::"n"(kDecThreads) : "memory");
+    if (lane == 0) {
 #pragma unroll
-  for (int g = 0; g < G; ++g)
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-#pragma unroll
-      for (int off = LPT; off < 32; off *= 2) o[g][i] += __shfl_xor_sync(0xffffffffu, o[g][i], off);
-
-  // every stage has landed and been read by all four warps: reuse stage memory
-  asm volatile("bar.sync 1, 160;" ::: "memory");
-  float* comb_o = reinterpret_cast<float*>(smem);       // [4][G][D]
-  float* comb_m = comb_o + 4 * G * D;                   // [4][G]
-  float* comb_l = comb_m + 4 * G;                       // [4][G]
-  if (tg == 0) {
+      for (int g = 0; g < G; ++g) {
+        comb_m[pair * G + g] = m_run[g];
+        comb_l[pair * G + g] = l_run[g];
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- PV
+    const int tg = lane / LPT;  // key slot within a warp step
+    const int ds = lane % LPT;  // 8-column slice
+    float2 o2[G][4];
 #pragma unroll
     for (int g = 0; g < G; ++g)
 #pragma unroll
-      for (int i = 0; i < 8; ++i) comb_o[(warp * G + g) * D + ds * 8 + i] = o[g][i];
+      for (int i = 0; i < 4; ++i) o2[g][i] = make_float2(0.f, 0.f);
+    for (int k = 0, j = pair; j < nstage; ++k, j += kDecPairs) {
+      const int st = j % kDecStages;
+      bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status);
+      if (ok) ok = mbar_wait(&pfull[pair], k & 1, abort_flag, p.status);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int nval = min(kDecTile, it.tok1 - (it.tok0 + j * kDecTile));
+      const uint8_t* vst = smem + st * C::STAGE + C::STAGE_K;
+      bool resc = false;
+      float al[G];
+#pragma unroll
+      for (int g = 0; g < G; ++g) {
+        al[g] = abuf[g];
+        resc |= (al[g] != 1.f);
+      }
+      if (resc) {
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o2[g][i] = __fmul2_rn(o2[g][i], make_float2(al[g], al[g]));
+      }
+#pragma unroll 4
+      for (int t = tg; t < nval; t += TPS) {
+        const uint4 vr = *reinterpret_cast<const uint4*>(vst + sw_off<D>(t, ds));
+        const float2 v2[4] = {Elt<T>::to_f2(vr.x), Elt<T>::to_f2(vr.y), Elt<T>::to_f2(vr.z), Elt<T>::to_f2(vr.w)};
+        float2 pp[G];
+#pragma unroll
+        for (int g = 0; g < G; g += 2) {
+          const float4 pv = *reinterpret_cast<const float4*>(pbuf + t * 8 + g);
+          pp[g] = make_float2(pv.x, pv.y);
+          if (g + 1 < G) pp[g + 1] = make_float2(pv.z, pv.w);
+        }
+#pragma unroll
+        for (int g = 0; g < G; ++g)
+#pragma unroll
+          for (int i = 0; i < 4; ++i) o2[g][i] = __ffma2_rn(pp[g], v2[i], o2[g][i]);
+      }
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&pempty[pair]);
+        mbar_arrive(&empty[st]);
+      }
+    }
+    // sum O over the TPS key slots of the warp
+#pragma unroll
+    for (int g = 0; g < G; ++g)
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int off = LPT; off < 32; off *= 2) {
+          o2[g][i].x += __shfl_xor_sync(0xffffffffu, o2[g][i].x, off);
+          o2[g][i].y += __shfl_xor_sync(0xffffffffu, o2[g][i].y, off);
+        }
+    // every stage has landed and been read: stage memory can be reused
+    asm volatile("bar.sync 1, %0;" ::"n"(kDecThreads) : "memory");
+    if (tg == 0) {
+#pragma unroll
+      for (int g = 0; g < G; ++g)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          *reinterpret_cast<float2*>(&comb_o[(pair * G + g) * D + ds * 8 + 2 * i]) = o2[g][i];
+    }
   }
-  if (lane < G) {
-    comb_m[warp * G + lane] = m_run;
-    comb_l[warp * G + lane] = l_run;
-  }
-  asm volatile("bar.sync 2, 128;" ::: "memory");
-  if (*abort_flag) return;
 
+  // ---------------------------------------------------------------- combine the pairs
+  asm volatile("bar.sync 2, %0;" ::"n"(64 * kDecPairs) : "memory");
+  if (*abort_flag) return;
   const bool partial = it.part_row >= 0;
-  for (int idx = tid; idx < G * D; idx += 128) {
+  for (int idx = tid; idx < G * D; idx += 64 * kDecPairs) {
     const int g = idx / D, d = idx % D;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, comb_m[w * G + g]);
+    for (int q = 0; q < kDecPairs; ++q) M = fmaxf(M, comb_m[q * G + g]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
     float L = 0.f, O = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float sc = ex2f(comb_m[w * G + g] - Mu);
-      L += sc * comb_l[w * G + g];
-      O += sc * comb_o[(w * G + g) * D + d];
+    for (int q = 0; q < kDecPairs; ++q) {
+      const float wq = ex2f(comb_m[q * G + g] - Mu);
+      L += wq * comb_l[q * G + g];
+      O += wq * comb_o[(q * G + g) * D + d];
     }
     const float val = L > 0.f ? O / L : 0.f;
     const float lse = L > 0.f ? (Mu + __log2f(L)) * kLn2f : -INFINITY;
@@ -392,7 +458,10 @@ cudaError_t launch_decode_t(const RunArgs& a, const CUtensorMap* map, const KPar
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  decode_kernel<T, D, G><<<a.hp->n_dec, kDecThreads, C::SMEM, a.stream>>>(*map, kp);
+  const int use_tma = (map != nullptr && a.hp->ps >= 8) ? 1 : 0;
+  CUtensorMap dummy;
+  if (!use_tma) memset(&dummy, 0, sizeof(dummy));
+  decode_kernel<T, D, G><<<a.hp->n_dec, kDecThreads, C::SMEM, a.stream>>>(use_tma ? *map : dummy, kp, use_tma);
   return cudaGetLastError();
 }
 

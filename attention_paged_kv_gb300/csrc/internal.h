@@ -73,6 +73,6 @@ struct pagedattn_plan_s {
   int force_cp_async = 0;
   // tensor maps over the last kv_cache pointer seen by run()
   const void* map_kv = nullptr;
-  CUtensorMap map_rows;   // decode: box {D, 1, min(ps, 64), 1}, no swizzle
+  CUtensorMap map_rows;   // decode: box {64, 1, min(ps, 64), 1}, 128-byte swizzle (page_size >= 8)
   CUtensorMap map_sw128;  // prefill: box {64, 1, ps, 1}, 128-byte swizzle
 };

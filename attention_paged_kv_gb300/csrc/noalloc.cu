@@ -80,9 +80,10 @@ extern "C" pagedattn_status pagedattn_run_decode_noalloc(pagedattn_plan_t plan, 
   pagedattn_status s = scratch_address(dev, &scratch);
   if (s != PA_OK) return s;
   CUtensorMap map;
-  s = encode_kv_map(&map, hp, kv_cache, uint32_t(hp.D), uint32_t(hp.ps < 64 ? hp.ps : 64),
-                    CU_TENSOR_MAP_SWIZZLE_NONE);
-  if (s != PA_OK) return s;
+  if (hp.ps >= 8) {
+    s = encode_kv_map(&map, hp, kv_cache, 64, uint32_t(hp.ps < 64 ? hp.ps : 64), CU_TENSOR_MAP_SWIZZLE_128B);
+    if (s != PA_OK) return s;
+  }
   cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
   // metadata (status word included, as zero) over whatever the last call left
   e = cudaMemcpyAsync(scratch, hp.blob.data(), hp.blob_bytes, cudaMemcpyHostToDevice, st);
@@ -96,7 +97,7 @@ extern "C" pagedattn_status pagedattn_run_decode_noalloc(pagedattn_plan_t plan, 
   a.out = out;
   a.lse = lse;
   a.stream = st;
-  e = launch_decode(a, &map);
+  e = launch_decode(a, hp.ps >= 8 ? &map : nullptr);
   if (e != cudaSuccess) return cuda_err(e, "no-alloc decode launch");
   e = launch_merge(a);
   if (e != cudaSuccess) return cuda_err(e, "no-alloc merge launch");
