@@ -76,6 +76,23 @@ pagedattn_status encode_kv_map(CUtensorMap* m, const pa::HostPlan& hp, const voi
   return PA_OK;
 }
 
+// 3-D view of q: (D, Hq, T), innermost first; box {64, G, 128 / G}: one
+// 128-row tile of packed (token, head) rows of one kv head, 128-byte swizzle.
+pagedattn_status encode_q_map(CUtensorMap* m, const pa::HostPlan& hp, const void* q) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return set_err(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  const cuuint64_t dims[3] = {cuuint64_t(hp.D), cuuint64_t(hp.Hq), cuuint64_t(hp.T)};
+  const cuuint64_t strides[2] = {cuuint64_t(hp.D) * 2, cuuint64_t(hp.Hq) * hp.D * 2};
+  const cuuint32_t box[3] = {64, cuuint32_t(hp.G), cuuint32_t(pa::kQRows / hp.G)};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUtensorMapDataType dt =
+      hp.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  CUresult r = fn(m, dt, 3, const_cast<void*>(q), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return set_err(PA_ERR_CUDA, "cuTensorMapEncodeTiled (q) failed, code " + std::to_string(int(r)));
+  return PA_OK;
+}
+
 }  // namespace pa
 
 using pa::encode_kv_map;
@@ -261,6 +278,11 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
     }
     plan->map_kv = kv_cache;
   }
+  if (hp.n_pre > 0 && q != plan->map_q_ptr) {
+    pagedattn_status s = pa::encode_q_map(&plan->map_q, hp, q);
+    if (s != PA_OK) return s;
+    plan->map_q_ptr = q;
+  }
   pa::RunArgs a;
   a.hp = &hp;
   a.workspace = plan->workspace;
@@ -271,7 +293,7 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.force_cp_async = plan->force_cp_async;
   if (stage_mask & PA_STAGE_PREFILL) {
-    e = pa::launch_prefill(a, hp.ps >= 8 ? &plan->map_sw128 : nullptr);
+    e = pa::launch_prefill(a, hp.ps >= 8 ? &plan->map_sw128 : nullptr, &plan->map_q);
     if (e != cudaSuccess) return cuda_err(e, "prefill launch");
   }
   if (stage_mask & PA_STAGE_DECODE) {

@@ -48,7 +48,7 @@ struct RunArgs {
   int force_cp_async;
 };
 
-cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128);
+cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const CUtensorMap* map_q);
 cudaError_t launch_decode(const RunArgs& a, const CUtensorMap* map_rows);
 cudaError_t launch_merge(const RunArgs& a);
 cudaError_t launch_debug_gather(const RunArgs& a, int32_t* page_out, int32_t* slot_out);
@@ -61,6 +61,7 @@ pagedattn_status cuda_err(cudaError_t e, const char* what);
 // box {box0, 1, box2, 1} (api.cu).
 pagedattn_status encode_kv_map(CUtensorMap* m, const HostPlan& hp, const void* kv, uint32_t box0, uint32_t box2,
                                CUtensorMapSwizzle sw);
+pagedattn_status encode_q_map(CUtensorMap* m, const HostPlan& hp, const void* q);
 
 }  // namespace pa
 
@@ -75,4 +76,7 @@ struct pagedattn_plan_s {
   const void* map_kv = nullptr;
   CUtensorMap map_rows;   // decode: box {64, 1, min(ps, 64), 1}, 128-byte swizzle (page_size >= 8)
   CUtensorMap map_sw128;  // prefill: box {64, 1, ps, 1}, 128-byte swizzle
+  // tensor map over the last q pointer seen by run() (prefill Q tiles)
+  const void* map_q_ptr = nullptr;
+  CUtensorMap map_q;
 };

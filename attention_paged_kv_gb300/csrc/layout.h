@@ -17,7 +17,8 @@ enum HdrIdx : int {
 
 constexpr int32_t kMagic = 0x50414731;
 constexpr int32_t kVersion = 1;
-constexpr int kQRows = 128;   // packed query rows per prefill tile
+constexpr int kQRows = 128;   // packed query rows per prefill MMA tile
+constexpr int kItemRows = 256;  // packed query rows per prefill work item (two tiles)
 constexpr int kKvTile = 128;  // keys per prefill key tile
 
 struct ReqEntry { int32_t qo_start, qo_len, kv_len, page_start; };

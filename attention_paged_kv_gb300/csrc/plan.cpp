@@ -14,11 +14,12 @@
 //     clamp(ceil(P_dec / (4 * SMs)), 256 keys, 2048 keys) in whole pages,
 //     P_dec = sum of decode pages x Hkv.  Each (request, kv head) is cut at
 //     multiples of the chunk.
-//  4. Prefill: tiles of 128 packed rows = 128/G tokens x G heads of one kv
-//     head (the G heads share every K/V tile load).  A tile needs keys
-//     [0, kv_b - qo_b + t0 + n) under the bottom-right causal mask; key tiles
-//     past that are never visited (the "skips the fully masked out tails" of
-//     the llama.cpp discussion "Pad for prefill stage?").  Split when the
+//  4. Prefill: items of 256 packed rows = 256/G tokens x G heads of one kv
+//     head, run as two 128-row MMA tiles that share every K/V tile load (as
+//     do the G heads).  An item needs keys [0, kv_b - qo_b + t0 + n) under
+//     the bottom-right causal mask; key tiles past that are never visited
+//     (the "skips the fully masked out tails" of the llama.cpp discussion
+//     "Pad for prefill stage?").  Split when the
 //     total key-tile count W exceeds 2 x SMs x chunk: chunk = max(8,
 //     ceil(W / (2 * SMs))) key tiles.
 //  5. Partial fp32 rows are numbered in emission order (decode splits, then
@@ -132,7 +133,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   }
 
   // -- rule 4: prefill items
-  const int32_t tq = kQRows / G;
+  const int32_t tq = kItemRows / G;
   struct Tile { int32_t b, t0, n; int64_t e; };
   std::vector<Tile> tiles;
   for (int b = 0; b < B; ++b) {

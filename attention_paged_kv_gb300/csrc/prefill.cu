@@ -1,49 +1,53 @@
 // Tensor-core prefill kernel over the paged KV cache (sm_103a: tcgen05 + TMEM).
 //
-// One CTA handles one work item: 128 packed query rows (128/G consecutive
-// tokens x the G query heads of one kv head, head-minor) of one request,
-// against the key range [kv_tok0, kv_tok1) of that request.  Packing the G
-// heads of a group into the MMA's M dimension makes every K/V tile load serve
-// all G heads (grouped-query attention has the higher operational intensity
-// the FlashInfer issue "How are prefill and decode kernels different?"
-// points out).  Key tiles wholly past the causal diagonal of the tile's last
-// row are never visited: the planner stops the range there ("skips the fully
-// masked out tails", llama.cpp discussion "Pad for prefill stage?").
+// One CTA handles one work item: 256 packed query rows -- 256/G consecutive
+// tokens x the G query heads of one kv head, head-minor -- of one request,
+// against the key range [kv_tok0, kv_tok1) of that request.  The rows form
+// two 128-row MMA tiles, A and B, that share every K/V tile load, as do the G
+// heads of a group (grouped-query attention has the higher operational
+// intensity the FlashInfer issue "How are prefill and decode kernels
+// different?" points out).  Key tiles wholly past the causal diagonal of the
+// item's last row are never visited: the planner stops the range there
+// ("skips the fully masked out tails", llama.cpp discussion "Pad for prefill
+// stage?").
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax / correction / epilogue; thread i owns row i, which is
-//              TMEM lane i, so the online softmax needs no shuffles.
-//   warp 4     producer: gathers the tile's pages through the page table with
-//              TMA (4-D tensor map over the cache, 128-byte swizzle), or with
-//              cp.async for pages smaller than 8 slots.
-//   warp 5     MMA issuer (one thread) and TMEM owner.
+// Warp roles (320 threads):
+//   warps 0-3  softmax / correction / epilogue of tile A; thread i owns row i
+//              = TMEM lane i, so the online softmax needs no shuffles.
+//   warps 4-7  the same for tile B.
+//   warp 8     producer: TMA loads of the two Q tiles (3-D map over q) and of
+//              each key tile's pages through the page table (4-D map over the
+//              cache, 128-byte swizzle), or cp.async for pages of < 8 slots.
+//   warp 9     MMA issuer (one thread) and TMEM owner.
 //
-// TMEM (512 columns): S double buffer at columns 0 and 128 (fp32 128x128),
-// O at column 256 (fp32 128xD).  P goes through shared memory as the A
-// operand of the second MMA.
+// TMEM (512 columns): S_A at 0, S_B at 128 (fp32 128x128), O_A at 256, O_B at
+// 384 (fp32 128xD).  P (fp16/bf16, two per column) is written over the first
+// 64 columns of its S and feeds the PV MMA as a TMEM A operand.
 //
-// Per key tile j:  S_j = Q K_j^T (tcgen05, both K-major) -> softmax threads
-// load S_j, mask the diagonal / tail, update the running max m and sum l,
-// write P_j (fp16/bf16) -> O += P_j V_j (V as an MN-major B operand).  The
-// running max is only moved (and O rescaled in TMEM) when it grows by more
-// than 8 in log2 units; p stays below 2^8 in between, which fp32 sums and
-// fp16/bf16 P carry without loss of range.  S_{j+1} is issued before PV_j so
-// the tensor core works while the softmax threads run.
+// Per key tile j the MMA thread issues, in order:
+//   PV_A(j) ; S_A(j+1) ; PV_B(j) ; S_B(j+1)
+// so while the softmax warps of one tile turn S into P, the tensor core works
+// on the other tile.  Softmax per tile: pass 1 reads S from TMEM in 32-column
+// chunks for the row max, pass 2 re-reads it for exp2, the row sum and P.
+// The running max is only moved (and O rescaled in TMEM) when it grows by
+// more than 8 in log2 units; p stays below 2^8 in between, which fp32 sums
+// and fp16/bf16 P carry without loss of range.
 //
 // Rows that see only a handful of keys average nothing out, so the 8-bit
 // mantissa of a bf16 P would show in their output.  All such rows sit in the
-// first key tile of a sequence; there P is written as hi + lo (two fp16/bf16
-// halves, lo = p - hi) and PV is issued for both, which gives P about 16
-// mantissa bits where it matters for one extra MMA set per item.
+// first key tile of a sequence; there P is split into hi (TMEM) + lo = p - hi
+// (shared memory) and PV is issued for both, which gives P about 16 mantissa
+// bits where it matters.
+#include <cstring>
+
 #include "common.cuh"
 #include "internal.h"
 
 namespace pa {
 namespace {
 
-constexpr int kPreThreads = 192;
+constexpr int kPreThreads = 320;
 constexpr uint32_t kTmemCols = 512;
-constexpr int kColS0 = 0, kColO = 256;
 constexpr float kLn2 = 0.6931471805599453f;
 
 template <int D>
@@ -51,15 +55,18 @@ struct PreCfg {
   static constexpr int NKB = D / 64;                 // 128-byte column blocks of a row
   static constexpr int NST = (D == 128) ? 2 : 4;     // K/V pipeline stages
   static constexpr int BLK = 128 * 128;              // one 128-row x 128-byte block
-  static constexpr int Q_BYTES = NKB * BLK;
+  static constexpr int Q_BYTES = NKB * BLK;          // one 128-row Q tile
   static constexpr int KV_BYTES = NKB * BLK;         // 128 keys of K (or V)
   static constexpr int P_BYTES = 2 * BLK;            // 128 rows x 128 keys x 2 bytes
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_K = OFF_Q + Q_BYTES;
+  static constexpr int OFF_Q = 0;                    // tiles A, B
+  static constexpr int OFF_K = 2 * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
-  static constexpr int OFF_P = OFF_V + NST * KV_BYTES;
-  static constexpr int OFF_PLO = OFF_P + P_BYTES;    // low half of split P (first key tile)
-  static constexpr int OFF_BAR = OFF_PLO + P_BYTES;
+  static constexpr int OFF_FREE = OFF_V + NST * KV_BYTES;
+  // P_lo buffers for the first key tile: tile A reuses K stage 0 when it is
+  // large enough (its keys are consumed by both S MMAs before P is written)
+  static constexpr int OFF_PLO_A = (KV_BYTES >= P_BYTES) ? OFF_K : OFF_FREE;
+  static constexpr int OFF_PLO_B = (KV_BYTES >= P_BYTES) ? OFF_FREE : OFF_FREE + P_BYTES;
+  static constexpr int OFF_BAR = OFF_PLO_B + P_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + alignment slack
 };
 
@@ -85,36 +92,47 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
+__device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
+  float m[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    m[i] = fmaxf(fmaxf(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])),
+                 fmaxf(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
+  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kPreThreads, 1)
-    prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p, const int use_tma) {
+    prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
+                   const KParams p, const int use_tma) {
   using C = PreCfg<D>;
   constexpr int NKB = C::NKB, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
   uint8_t* smem = smem_raw + ((1024u - (raw_addr & 1023u)) & 1023u);
   const uint32_t sbase = smem_u32(smem);
-  const uint32_t q_addr = sbase + C::OFF_Q;
-  const uint32_t p_addr = sbase + C::OFF_P;
-  const uint32_t plo_addr = sbase + C::OFF_PLO;
+  auto q_addr = [&](int x) { return sbase + C::OFF_Q + x * C::Q_BYTES; };
   auto k_addr = [&](int st) { return sbase + C::OFF_K + st * C::KV_BYTES; };
   auto v_addr = [&](int st) { return sbase + C::OFF_V + st * C::KV_BYTES; };
+  auto plo_off = [&](int x) { return x == 0 ? C::OFF_PLO_A : C::OFF_PLO_B; };
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* full = bars;              // [NST] K/V tile landed
-  uint64_t* empty = bars + NST;       // [NST] PV MMA done with the stage
-  uint64_t* s_full = bars + 2 * NST;  // [2] S MMA done
-  uint64_t* s_free = s_full + 2;      // [2] softmax warps have read S
-  uint64_t* p_full = s_free + 2;      // P (and O correction) written
-  uint64_t* o_done = p_full + 1;      // PV MMA done
-  uint64_t* q_full = o_done + 1;      // Q staged
-  uint64_t* fin = q_full + 1;         // all MMAs retired (teardown)
+  uint64_t* full = bars;                // [NST] K/V tile landed
+  uint64_t* empty = bars + NST;         // [NST] both PV MMAs done with the stage
+  uint64_t* q_full = bars + 2 * NST;    // both Q tiles landed
+  uint64_t* s_full = q_full + 1;        // [2] S_x MMA done
+  uint64_t* p_full = s_full + 2;        // [2] P_x (and O_x correction) written
+  uint64_t* o_done = p_full + 2;        // [2] PV_x MMA done
+  uint64_t* fin = o_done + 2;           // all MMAs retired (teardown)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PreItem it = p.pre[blockIdx.x];
   const ReqEntry rq = p.req[it.req];
+  const int G = p.G;
+  const int TQ = kQRows >> p.g_shift;           // tokens per 128-row tile
+  const bool has_b = it.q_ntok > TQ;
   const int nkt = (it.kv_tok1 - it.kv_tok0 + kKvTile - 1) / kKvTile;
   // split P on the first key tile when some row of the item sees < 128 keys
   const int first_vis = p.causal ? (rq.kv_len - rq.qo_len + it.q_tok0 + 1) : rq.kv_len;
@@ -125,26 +143,36 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       mbar_init(&full[i], use_tma ? 1 : 32);
       mbar_init(&empty[i], 1);
     }
+    mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&o_done[i], 1);
     }
-    mbar_init(p_full, 4);
-    mbar_init(o_done, 1);
-    mbar_init(q_full, 4);
     mbar_init(fin, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 5) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == 9) tmem_alloc(tmem_slot, kTmemCols);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------------------------------------------------------- producer
-    if (use_tma && lane == 0) tma_prefetch_desc(&kv_map);
+    if (lane == 0) {
+      tma_prefetch_desc(&q_map);
+      if (use_tma) tma_prefetch_desc(&kv_map);
+      mbar_arrive_expect_tx(q_full, uint32_t((has_b ? 2 : 1) * C::Q_BYTES));
+#pragma unroll
+      for (int kb = 0; kb < NKB; ++kb) {
+        tma_load_3d(q_addr(0) + kb * C::BLK, &q_map, kb * 64, it.kv_head * G, rq.qo_start + it.q_tok0, q_full);
+        if (has_b)
+          tma_load_3d(q_addr(1) + kb * C::BLK, &q_map, kb * 64, it.kv_head * G, rq.qo_start + it.q_tok0 + TQ,
+                      q_full);
+      }
+    }
     const int ps = p.ps, sh = p.ps_shift;
     int issued = 0;
     for (int j = 0; j < nkt; ++j) {
@@ -213,55 +241,73 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       issued = j + 1;
     }
     // drain: copies still in flight must land before the CTA's memory goes away
-    if (use_tma && lane == 0) {
-      for (int j = max(0, issued - NST); j < issued; ++j) drain_wait(&full[j % NST], (j / NST) & 1);
+    if (lane == 0) {
+      drain_wait(q_full, 0);
+      if (use_tma)
+        for (int j = max(0, issued - NST); j < issued; ++j) drain_wait(&full[j % NST], (j / NST) & 1);
     }
     __syncwarp();
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_f16(Elt<T>::kBf16, 0, 0, 128, 128);
       const uint32_t id_o = idesc_f16(Elt<T>::kBf16, 0, 1, 128, D);
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
-      tc_fence_after();
-      for (int j = 0; ok && j <= nkt; ++j) {
-        if (j < nkt) {
-          const int st = j % NST;
-          ok = mbar_wait(&full[st], (j / NST) & 1, abort_flag, p.status);
-          if (ok && j >= 2) ok = mbar_wait(&s_free[j & 1], ((j >> 1) - 1) & 1, abort_flag, p.status);
-          if (!ok) break;
-          tc_fence_after();
-          const uint32_t d = tmem + kColS0 + (j & 1) * 128;
+      auto issue_s = [&](int x, int st) {
+        const uint32_t d = tmem + x * 128;
 #pragma unroll
-          for (int k = 0; k < D / 16; ++k) {
-            const uint32_t koff = (k >> 2) * C::BLK + (k & 3) * 32;
-            tc_mma_ss(d, smem_desc_sw128(q_addr + koff, 16, 1024), smem_desc_sw128(k_addr(st) + koff, 16, 1024),
-                      id_s, k > 0 ? 1u : 0u);
-          }
-          tc_commit(&s_full[j & 1]);
+        for (int k = 0; k < D / 16; ++k) {
+          const uint32_t koff = (k >> 2) * C::BLK + (k & 3) * 32;
+          tc_mma_ss(d, smem_desc_sw128(q_addr(x) + koff, 16, 1024), smem_desc_sw128(k_addr(st) + koff, 16, 1024),
+                    id_s, k > 0 ? 1u : 0u);
         }
-        if (j >= 1) {
-          const int i = j - 1, st = i % NST;
-          ok = mbar_wait(p_full, i & 1, abort_flag, p.status);
-          if (!ok) break;
-          tc_fence_after();
+        tc_commit(&s_full[x]);
+      };
+      auto issue_pv = [&](int x, int j, int st) {
+        const uint32_t d = tmem + 256 + x * 128;
+#pragma unroll
+        for (int k = 0; k < kKvTile / 16; ++k)
+          tc_mma_ts(d, tmem + x * 128 + k * 8, smem_desc_sw128(v_addr(st) + k * 2048, C::BLK, 1024), id_o,
+                    (j > 0 || k > 0) ? 1u : 0u);
+        if (j == 0 && lo_split0) {
+          const uint32_t lo = sbase + plo_off(x);
 #pragma unroll
           for (int k = 0; k < kKvTile / 16; ++k) {
             const uint32_t aoff = (k >> 2) * C::BLK + (k & 3) * 32;
-            tc_mma_ss(tmem + kColO, smem_desc_sw128(p_addr + aoff, 16, 1024),
-                      smem_desc_sw128(v_addr(st) + k * 2048, C::BLK, 1024), id_o, (i > 0 || k > 0) ? 1u : 0u);
+            tc_mma_ss(d, smem_desc_sw128(lo + aoff, 16, 1024), smem_desc_sw128(v_addr(st) + k * 2048, C::BLK, 1024),
+                      id_o, 1u);
           }
-          if (i == 0 && lo_split0) {
-#pragma unroll
-            for (int k = 0; k < kKvTile / 16; ++k) {
-              const uint32_t aoff = (k >> 2) * C::BLK + (k & 3) * 32;
-              tc_mma_ss(tmem + kColO, smem_desc_sw128(plo_addr + aoff, 16, 1024),
-                        smem_desc_sw128(v_addr(st) + k * 2048, C::BLK, 1024), id_o, 1u);
-            }
-          }
-          tc_commit(&empty[st]);
-          tc_commit(o_done);
         }
+        tc_commit(&o_done[x]);
+      };
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
+      if (ok) ok = mbar_wait(&full[0], 0, abort_flag, p.status);
+      if (ok) {
+        tc_fence_after();
+        issue_s(0, 0);
+        if (has_b) issue_s(1, 0);
+      }
+      for (int j = 0; ok && j < nkt; ++j) {
+        const int st = j % NST;
+        const bool more = j + 1 < nkt;
+        const int st1 = (j + 1) % NST;
+        ok = mbar_wait(&p_full[0], j & 1, abort_flag, p.status);
+        if (!ok) break;
+        tc_fence_after();
+        issue_pv(0, j, st);
+        if (more) {
+          ok = mbar_wait(&full[st1], ((j + 1) / NST) & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(0, st1);
+        }
+        if (has_b) {
+          ok = mbar_wait(&p_full[1], j & 1, abort_flag, p.status);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(1, j, st);
+        }
+        tc_commit(&empty[st]);
+        if (has_b && more) issue_s(1, st1);
       }
       tc_commit(fin);
       drain_wait(fin, 0);
@@ -269,71 +315,43 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     __syncwarp();
   } else {
     // ---------------------------------------------------------------- softmax warps
-    const int r = tid;
-    const int G = p.G;
+    const int x = warp >> 2;                       // tile
+    const int r = tid & 127;                       // row = TMEM lane
     const int tok_local = r >> p.g_shift;
     const int g = r & (G - 1);
-    const bool row_valid = tok_local < it.q_ntok;
-    const int qi = it.q_tok0 + tok_local;
+    const bool row_valid = (x * TQ + tok_local) < it.q_ntok && (x == 0 || has_b);
+    const int qi = it.q_tok0 + x * TQ + tok_local;
     const int64_t qrow = (int64_t(rq.qo_start) + qi) * p.Hq + int64_t(it.kv_head) * G + g;
-
-    {  // stage this row of Q (zeros for rows past the tile)
-      const T* qsrc = static_cast<const T*>(p.q) + (row_valid ? qrow * D : 0);
-#pragma unroll
-      for (int kb = 0; kb < NKB; ++kb)
-#pragma unroll
-        for (int c = 0; c < 8; ++c)
-          cp_async16(q_addr + kb * C::BLK + r * 128 + ((c ^ (r & 7)) * 16), qsrc + (row_valid ? kb * 64 + c * 8 : 0),
-                     row_valid ? 16u : 0u);
-      cp_async_commit();
-      cp_async_wait_all();
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(q_full);
-    }
-
     int row_end = p.causal ? (rq.kv_len - rq.qo_len + qi + 1) : rq.kv_len;
     row_end = min(row_end, it.kv_tok1);
     if (!row_valid) row_end = 0;
     const float sl2 = p.scale_log2;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_col = tmem + lane_base + x * 128;
+    const uint32_t o_col = tmem + lane_base + 256 + x * 128;
     float m_ref = -INFINITY, l_sum = 0.f;
-    const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-    bool ok = true;
+    bool ok = (x == 0) || has_b;
 
-    for (int j = 0; j < nkt; ++j) {
+    for (int j = 0; ok && j < nkt; ++j) {
       const int k0 = it.kv_tok0 + j * kKvTile;
-      ok = warp_wait(&s_full[j & 1], (j >> 1) & 1, abort_flag, p.status);
+      ok = warp_wait(&s_full[x], j & 1, abort_flag, p.status);
       if (!ok) break;
       tc_fence_after();
-      uint32_t s[128];
-      const uint32_t sa = tmem + lane_base + kColS0 + (j & 1) * 128;
-      tmem_ld32(sa + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
-      tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
-      tmem_ld32(sa + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
-      tmem_ld32(sa + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
-      tmem_wait_ld();
-#pragma unroll
-      for (int i = 0; i < 128; ++i) asm volatile("" : "+r"(s[i]));
-      const bool lo_split = lo_split0 && j == 0;
-      if (!lo_split) {
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[j & 1]);
-      }
-
-      // mask (diagonal / tail tiles only) and tile max
       const int lim = row_end - k0;
+
+      // pass 1: row max over the 128 columns (masked past the row's end)
       float mx = -INFINITY;
-      if (lim >= kKvTile) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) mx = fmaxf(mx, __uint_as_float(s[c]));
-      } else {
+      for (int c = 0; c < 4; ++c) {
+        uint32_t s[32];
+        tmem_ld32(s_col + c * 32, s);
+        tmem_wait_ld(s);
+        if (lim < kKvTile) {
 #pragma unroll
-        for (int c = 0; c < 128; ++c) {
-          const float v = (c < lim) ? __uint_as_float(s[c]) : -INFINITY;
-          s[c] = __float_as_uint(v);
-          mx = fmaxf(mx, v);
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i >= lim) s[i] = __float_as_uint(-INFINITY);
         }
+        mx = fmaxf(mx, max32(s));
       }
       const float mx2 = mx * sl2;
       float alpha = 1.f;
@@ -346,20 +364,10 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         m_ref = mx2;
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float rs = 0.f;
-      uint32_t pw[64];
-#pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        const float a = ex2(fmaf(__uint_as_float(s[2 * c]), sl2, -m_use));
-        const float b = ex2(fmaf(__uint_as_float(s[2 * c + 1]), sl2, -m_use));
-        rs += a + b;
-        pw[c] = Elt<T>::from_f2(a, b);
-      }
-      l_sum = l_sum * alpha + rs;
 
-      // PV of the previous tile must be done before P and O are touched
+      // PV of the previous tile must be done before O is rescaled
       if (j >= 1) {
-        ok = warp_wait(o_done, (j - 1) & 1, abort_flag, p.status);
+        ok = warp_wait(&o_done[x], (j - 1) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
       }
@@ -367,17 +375,16 @@ __global__ void __launch_bounds__(kPreThreads, 1)
 #pragma unroll
         for (int c4 = 0; c4 < D / 32; ++c4) {
           uint32_t o[32];
-          tmem_ld32(tmem + lane_base + kColO + c4 * 32, o);
+          tmem_ld32(o_col + c4 * 32, o);
           tmem_wait_ld(o);
 #pragma unroll
           for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(tmem + lane_base + kColO + c4 * 32, o);
+          tmem_st32(o_col + c4 * 32, o);
         }
-        tmem_wait_st();
       }
       // keys past the end of the range: zero their V rows (they may hold
       // anything, and 0 * NaN would poison O); cp.async already zero-filled
-      if (use_tma && j == nkt - 1) {
+      if (x == 0 && use_tma && j == nkt - 1) {
         const int valid = it.kv_tok1 - k0;
         if (valid < kKvTile) {
           const int st = j % NST;
@@ -393,56 +400,63 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           }
         }
       }
-      // P row -> shared memory, K-major with the 128-byte swizzle
-#pragma unroll
-      for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-        for (int c = 0; c < 8; ++c) {
-          uint4 v = make_uint4(pw[kb * 32 + c * 4 + 0], pw[kb * 32 + c * 4 + 1], pw[kb * 32 + c * 4 + 2],
-                               pw[kb * 32 + c * 4 + 3]);
-          *reinterpret_cast<uint4*>(smem + C::OFF_P + kb * C::BLK + r * 128 + ((c ^ (r & 7)) * 16)) = v;
-        }
-      if (lo_split) {
-        // second pass over S (still in TMEM: its buffer is only released
-        // below): the same p values again, minus their rounded high halves
-        tmem_ld32(sa + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
-        tmem_ld32(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
-        tmem_ld32(sa + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
-        tmem_ld32(sa + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
-        tmem_wait_ld();
-#pragma unroll
-        for (int i = 0; i < 128; ++i) asm volatile("" : "+r"(s[i]));
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&s_free[j & 1]);
-#pragma unroll
-        for (int kb = 0; kb < 2; ++kb)
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            uint32_t lw[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int col = kb * 64 + c * 8 + 2 * u;
-              const float va = (col < lim) ? __uint_as_float(s[col]) : -INFINITY;
-              const float vb = (col + 1 < lim) ? __uint_as_float(s[col + 1]) : -INFINITY;
-              const float a = ex2(fmaf(va, sl2, -m_use));
-              const float b = ex2(fmaf(vb, sl2, -m_use));
-              const float2 hi = Elt<T>::to_f2(Elt<T>::from_f2(a, b));
-              lw[u] = Elt<T>::from_f2(a - hi.x, b - hi.y);
-            }
-            *reinterpret_cast<uint4*>(smem + C::OFF_PLO + kb * C::BLK + r * 128 + ((c ^ (r & 7)) * 16)) =
-                make_uint4(lw[0], lw[1], lw[2], lw[3]);
-          }
+      const bool lo_split = lo_split0 && j == 0;
+      if (lo_split && x == 0 && C::OFF_PLO_A == C::OFF_K && has_b) {
+        // tile A's P_lo reuses K stage 0: S_B(0) must be done reading it
+        ok = warp_wait(&s_full[1], 0, abort_flag, p.status);
+        if (!ok) break;
       }
+
+      // pass 2: p = exp2(s * scale_log2 - m), row sum, P (hi) into TMEM over S
+      const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
+      float rs = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t s[32];
+        tmem_ld32(s_col + c * 32, s);
+        tmem_wait_ld(s);
+        if (lim < kKvTile) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i)
+            if (c * 32 + i >= lim) s[i] = __float_as_uint(-INFINITY);
+        }
+        uint32_t ph[16];
+        float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+          const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), sc2, nm2);
+          const float a = ex2(t2.x), b = ex2(t2.y);
+          acc2 = __fadd2_rn(acc2, make_float2(a, b));
+          ph[i] = Elt<T>::from_f2(a, b);
+          if (lo_split) {
+            const float2 hi = Elt<T>::to_f2(ph[i]);
+            s[2 * i] = Elt<T>::from_f2(a - hi.x, b - hi.y);   // reuse s[] for the lo words
+          }
+        }
+        rs += acc2.x + acc2.y;
+        tmem_st16(s_col + c * 16, ph);
+        if (lo_split) {
+          // keys 32c .. 32c+31 of row r -> K-major 128-byte-swizzled smem
+          uint8_t* base = smem + plo_off(x) + (c >> 1) * C::BLK + r * 128;
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const int cc = (c & 1) * 4 + u;
+            *reinterpret_cast<uint4*>(base + ((cc ^ (r & 7)) * 16)) =
+                make_uint4(s[8 * u], s[8 * u + 2], s[8 * u + 4], s[8 * u + 6]);
+          }
+        }
+      }
+      l_sum = l_sum * alpha + rs;
+      tmem_wait_st();
       fence_proxy_async_smem();
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(p_full);
+      if (lane == 0) mbar_arrive(&p_full[x]);
     }
 
     // ---------------------------------------------------------------- epilogue
-    if (ok) ok = warp_wait(o_done, (nkt - 1) & 1, abort_flag, p.status);
-    if (ok) {
+    if (ok && (x == 0 || has_b)) ok = warp_wait(&o_done[x], (nkt - 1) & 1, abort_flag, p.status);
+    if (ok && (x == 0 || has_b)) {
       tc_fence_after();
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
       const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
@@ -451,7 +465,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
 #pragma unroll
       for (int c4 = 0; c4 < D / 32; ++c4) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_base + kColO + c4 * 32, o);
+        tmem_ld32(o_col + c4 * 32, o);
         tmem_wait_ld(o);
         if (row_valid) {
           if (!partial) {
@@ -466,7 +480,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
               dst[v] = w;
             }
           } else {
-            float4* dst = reinterpret_cast<float4*>(p.part_o + (int64_t(it.part_row) + r) * D + c4 * 32);
+            float4* dst =
+                reinterpret_cast<float4*>(p.part_o + (int64_t(it.part_row) + x * kQRows + r) * D + c4 * 32);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               dst[v] = make_float4(__uint_as_float(o[4 * v + 0]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
@@ -478,7 +493,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         if (!partial) {
           if (p.lse) p.lse[qrow] = lse_v;
         } else {
-          p.part_lse[it.part_row + r] = lse_v;
+          p.part_lse[it.part_row + x * kQRows + r] = lse_v;
         }
       }
     }
@@ -487,14 +502,15 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 5) {
+  if (warp == 9) {
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
 }
 
 template <typename T, int D>
-cudaError_t launch_prefill_t(const RunArgs& a, const CUtensorMap* map, const KParams& kp, int use_tma) {
+cudaError_t launch_prefill_t(const RunArgs& a, const CUtensorMap* kv_map, const CUtensorMap* q_map,
+                             const KParams& kp, int use_tma) {
   using C = PreCfg<D>;
   static bool attr_set = false;
   if (!attr_set) {
@@ -502,7 +518,7 @@ cudaError_t launch_prefill_t(const RunArgs& a, const CUtensorMap* map, const KPa
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  prefill_kernel<T, D><<<a.hp->n_pre, kPreThreads, C::SMEM, a.stream>>>(*map, kp, use_tma);
+  prefill_kernel<T, D><<<a.hp->n_pre, kPreThreads, C::SMEM, a.stream>>>(*kv_map, *q_map, kp, use_tma);
   return cudaGetLastError();
 }
 
@@ -510,18 +526,20 @@ cudaError_t launch_prefill_t(const RunArgs& a, const CUtensorMap* map, const KPa
 
 KParams make_params(const RunArgs& a);
 
-cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128) {
+cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const CUtensorMap* map_q) {
   if (a.hp->n_pre == 0) return cudaSuccess;
   KParams kp = make_params(a);
   kp.n_items = a.hp->n_pre;
   const int use_tma = (map_sw128 != nullptr && !a.force_cp_async && a.hp->ps >= 8) ? 1 : 0;
   CUtensorMap dummy;
+  memset(&dummy, 0, sizeof(dummy));
   const CUtensorMap* m = use_tma ? map_sw128 : &dummy;
-  if (!use_tma) memset(&dummy, 0, sizeof(dummy));
   const bool bf = a.hp->dtype == PA_BF16;
   if (a.hp->D == 128)
-    return bf ? launch_prefill_t<__nv_bfloat16, 128>(a, m, kp, use_tma) : launch_prefill_t<__half, 128>(a, m, kp, use_tma);
-  return bf ? launch_prefill_t<__nv_bfloat16, 64>(a, m, kp, use_tma) : launch_prefill_t<__half, 64>(a, m, kp, use_tma);
+    return bf ? launch_prefill_t<__nv_bfloat16, 128>(a, m, map_q, kp, use_tma)
+              : launch_prefill_t<__half, 128>(a, m, map_q, kp, use_tma);
+  return bf ? launch_prefill_t<__nv_bfloat16, 64>(a, m, map_q, kp, use_tma)
+            : launch_prefill_t<__half, 64>(a, m, map_q, kp, use_tma);
 }
 
 }  // namespace pa

@@ -21,9 +21,10 @@ Rules (the planner is deterministic; nothing depends on timing):
    clamp(ceil(P_dec / target), max(1, 256 // page_size), max(1, 2048 // page_size))
    pages (or the override).  Request b is cut into ceil(pages_b / chunk)
    splits at page boundaries, for every kv head.
-4. Prefill tiles: 128 packed rows = (128 / G) query tokens x G heads.  Tile
-   [t0, t0 + n) of request b needs keys [0, e) with e = kv_b - qo_b + t0 + n
-   (causal) or kv_b; that is ceil(e / 128) key tiles of 128.  With W = the
+4. Prefill items: 256 packed rows = (256 / G) query tokens x G heads (two
+   128-row tiles).  Item [t0, t0 + n) of request b needs keys [0, e) with
+   e = kv_b - qo_b + t0 + n (causal) or kv_b; that is ceil(e / 128) key
+   tiles of 128.  With W = the
    sum of key tiles over all (tile, kv head) items and target = 2 * num_sms,
    the chunk is max(8, ceil(W / target)) key tiles (or the override); an item
    with more key tiles is cut into ceil(tiles / chunk) splits.
@@ -61,7 +62,8 @@ MAGIC = 0x50414731
 VERSION = 1
 HDR_WORDS = 64
 STATUS_WORD = 32
-Q_ROWS = 128       # packed query rows per prefill tile
+Q_ROWS = 128       # packed query rows per prefill MMA tile (G must divide it)
+ITEM_ROWS = 256    # packed query rows per prefill work item
 KV_TILE = 128      # keys per prefill key tile
 DEC_ITEMS_PER_SM = 4
 PRE_ITEMS_PER_SM = 2
@@ -140,7 +142,7 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
                 dec.append((b, h, t0, t1, base + s * G if ns > 1 else -1))
 
     # -- prefill items (rule 4)
-    tq = Q_ROWS // G
+    tq = ITEM_ROWS // G
     tiles = []  # (b, t0, n, e)
     for b, ((qo, kv, p0, npg), d) in enumerate(zip(lens, is_dec)):
         if d or qo == 0:

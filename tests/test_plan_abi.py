@@ -189,9 +189,9 @@ def test_plan_metadata_semantics(lib):
     w = workloads.decode()
     h = plan_ref.decode_header(_lib_blob(w, num_sms=148))
     assert (h["n_dec"], h["n_pre"], h["n_merge"], h["dec_chunk_pages"]) == (512, 0, 128, 16)
-    w = workloads.mixed(num_decode=8, prefill_len=2048, kv_lo=512, kv_hi=8192)
+    w = workloads.mixed(num_decode=8, prefill_len=8192, kv_lo=512, kv_hi=8192)
     blob = _lib_blob(w, num_sms=148)
     dec, pre, mer = plan_ref.items(blob)
     assert (pre[:, 6] == -1).all()                 # no prefill split
-    assert pre[:, 3].max() == 16                   # 16 tokens x 8 heads per tile
-    assert pre[0, 5] - pre[0, 4] == 2048           # longest first
+    assert pre[:, 3].max() == 32                   # 32 tokens x 8 heads per item (two tiles)
+    assert pre[0, 5] - pre[0, 4] == 8192           # longest first
