@@ -27,8 +27,8 @@
 // Per key tile j the MMA thread issues, in order:
 //   PV_A(j) ; S_A(j+1) ; PV_B(j) ; S_B(j+1)
 // so while the softmax warps of one tile turn S into P, the tensor core works
-// on the other tile.  Softmax per tile: pass 1 reads S from TMEM in 32-column
-// chunks for the row max, pass 2 re-reads it for exp2, the row sum and P.
+// on the other tile.  Softmax per tile: the S row is read from TMEM into
+// registers (four loads, one wait), then max, exp2, the row sum and P.
 // The running max is only moved (and O rescaled in TMEM) when it grows by
 // more than 8 in log2 units; p stays below 2^8 in between, which fp32 sums
 // and fp16/bf16 P carry without loss of range.
@@ -339,20 +339,24 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       tc_fence_after();
       const int lim = row_end - k0;
 
-      // pass 1: row max over the 128 columns (masked past the row's end)
-      float mx = -INFINITY;
+      // the whole S row in registers: four loads, one wait
+      uint32_t s[128];
+      tmem_ld32(s_col + 0, *reinterpret_cast<uint32_t(*)[32]>(s + 0));
+      tmem_ld32(s_col + 32, *reinterpret_cast<uint32_t(*)[32]>(s + 32));
+      tmem_ld32(s_col + 64, *reinterpret_cast<uint32_t(*)[32]>(s + 64));
+      tmem_ld32(s_col + 96, *reinterpret_cast<uint32_t(*)[32]>(s + 96));
+      tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t s[32];
-        tmem_ld32(s_col + c * 32, s);
-        tmem_wait_ld(s);
-        if (lim < kKvTile) {
+      for (int i = 0; i < 128; ++i) asm volatile("" : "+r"(s[i]));
+      if (lim < kKvTile) {  // mask past the row's end (diagonal / tail tiles only)
 #pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= lim) s[i] = __float_as_uint(-INFINITY);
-        }
-        mx = fmaxf(mx, max32(s));
+        for (int i = 0; i < 128; ++i)
+          if (i >= lim) s[i] = __float_as_uint(-INFINITY);
       }
+      float mx = fmaxf(fmaxf(max32(*reinterpret_cast<uint32_t(*)[32]>(s + 0)),
+                             max32(*reinterpret_cast<uint32_t(*)[32]>(s + 32))),
+                       fmaxf(max32(*reinterpret_cast<uint32_t(*)[32]>(s + 64)),
+                             max32(*reinterpret_cast<uint32_t(*)[32]>(s + 96))));
       const float mx2 = mx * sl2;
       float alpha = 1.f;
       bool resc = false;
@@ -365,6 +369,46 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
 
+      const bool lo_split = lo_split0 && j == 0;
+      if (lo_split && x == 0 && C::OFF_PLO_A == C::OFF_K && has_b) {
+        // tile A's P_lo reuses K stage 0: S_B(0) must be done reading it
+        ok = warp_wait(&s_full[1], 0, abort_flag, p.status);
+        if (!ok) break;
+      }
+
+      // p = exp2(s * scale_log2 - m), row sum, P (hi) into TMEM over S
+      const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
+      float2 acc2 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t ph[16];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint32_t lw[4];
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int i = 4 * u + v, k = 32 * c + 2 * i;
+            const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), sc2, nm2);
+            const float a = ex2(t2.x), b = ex2(t2.y);
+            acc2 = __fadd2_rn(acc2, make_float2(a, b));
+            ph[i] = Elt<T>::from_f2(a, b);
+            if (lo_split) {
+              const float2 hi = Elt<T>::to_f2(ph[i]);
+              lw[v] = Elt<T>::from_f2(a - hi.x, b - hi.y);
+            }
+          }
+          if (lo_split) {
+            // keys 32c + 8u .. +7 of row r -> K-major 128-byte-swizzled smem
+            const int cc = (c & 1) * 4 + u;
+            *reinterpret_cast<uint4*>(smem + plo_off(x) + (c >> 1) * C::BLK + r * 128 + ((cc ^ (r & 7)) * 16)) =
+                make_uint4(lw[0], lw[1], lw[2], lw[3]);
+          }
+        }
+        tmem_st16(s_col + c * 16, ph);
+      }
+      const float rs = acc2.x + acc2.y;
+      // S_x(j) done implies PV_x(j-1) done (the MMAs run in issue order); the
+      // barrier makes O's contents visible before it is rescaled
       // PV of the previous tile must be done before O is rescaled
       if (j >= 1) {
         ok = warp_wait(&o_done[x], (j - 1) & 1, abort_flag, p.status);
@@ -397,52 +441,6 @@ __global__ void __launch_bounds__(kPreThreads, 1)
 #pragma unroll
               for (int c = 0; c < 8; ++c)
                 *reinterpret_cast<uint4*>(vrow + kb * C::BLK + c * 16) = make_uint4(0, 0, 0, 0);
-          }
-        }
-      }
-      const bool lo_split = lo_split0 && j == 0;
-      if (lo_split && x == 0 && C::OFF_PLO_A == C::OFF_K && has_b) {
-        // tile A's P_lo reuses K stage 0: S_B(0) must be done reading it
-        ok = warp_wait(&s_full[1], 0, abort_flag, p.status);
-        if (!ok) break;
-      }
-
-      // pass 2: p = exp2(s * scale_log2 - m), row sum, P (hi) into TMEM over S
-      const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
-      float rs = 0.f;
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t s[32];
-        tmem_ld32(s_col + c * 32, s);
-        tmem_wait_ld(s);
-        if (lim < kKvTile) {
-#pragma unroll
-          for (int i = 0; i < 32; ++i)
-            if (c * 32 + i >= lim) s[i] = __float_as_uint(-INFINITY);
-        }
-        uint32_t ph[16];
-        float2 acc2 = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(s[2 * i]), __uint_as_float(s[2 * i + 1])), sc2, nm2);
-          const float a = ex2(t2.x), b = ex2(t2.y);
-          acc2 = __fadd2_rn(acc2, make_float2(a, b));
-          ph[i] = Elt<T>::from_f2(a, b);
-          if (lo_split) {
-            const float2 hi = Elt<T>::to_f2(ph[i]);
-            s[2 * i] = Elt<T>::from_f2(a - hi.x, b - hi.y);   // reuse s[] for the lo words
-          }
-        }
-        rs += acc2.x + acc2.y;
-        tmem_st16(s_col + c * 16, ph);
-        if (lo_split) {
-          // keys 32c .. 32c+31 of row r -> K-major 128-byte-swizzled smem
-          uint8_t* base = smem + plo_off(x) + (c >> 1) * C::BLK + r * 128;
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int cc = (c & 1) * 4 + u;
-            *reinterpret_cast<uint4*>(base + ((cc ^ (r & 7)) * 16)) =
-                make_uint4(s[8 * u], s[8 * u + 2], s[8 * u + 4], s[8 * u + 6]);
           }
         }
       }
