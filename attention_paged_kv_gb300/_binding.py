@@ -56,7 +56,8 @@ class PagedAttnError(RuntimeError):
 class Options(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int32), ("force_prefill", ctypes.c_int32),
                 ("decode_chunk_pages", ctypes.c_int32), ("prefill_chunk_tiles", ctypes.c_int32),
-                ("force_cp_async", ctypes.c_int32), ("reserved", ctypes.c_int32 * 3)]
+                ("force_cp_async", ctypes.c_int32), ("decode_cuda_cores", ctypes.c_int32),
+                ("reserved", ctypes.c_int32 * 2)]
 
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
@@ -136,13 +137,14 @@ def dtype_code(dtype) -> int:
 
 
 def _options(num_sms=0, force_prefill=False, decode_chunk_pages=0, prefill_chunk_tiles=0,
-             force_cp_async=False) -> Options:
+             force_cp_async=False, decode_cuda_cores=False) -> Options:
     o = Options()
     o.num_sms = int(num_sms)
     o.force_prefill = int(bool(force_prefill))
     o.decode_chunk_pages = int(decode_chunk_pages)
     o.prefill_chunk_tiles = int(prefill_chunk_tiles)
     o.force_cp_async = int(bool(force_cp_async))
+    o.decode_cuda_cores = int(bool(decode_cuda_cores))
     return o
 
 

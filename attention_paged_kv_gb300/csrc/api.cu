@@ -119,7 +119,7 @@ pagedattn_status fill_inputs(pa::PlanInputs* in, const int32_t* qo_indptr, const
   pagedattn_options o;
   std::memset(&o, 0, sizeof(o));
   if (opts) o = *opts;
-  for (int i = 0; i < 3; ++i)
+  for (int i = 0; i < 2; ++i)
     if (o.reserved[i] != 0) return set_err(PA_ERR_INVALID_ARG, "pagedattn_options.reserved must be zero");
   if (o.num_sms < 0 || o.decode_chunk_pages < 0 || o.prefill_chunk_tiles < 0)
     return set_err(PA_ERR_INVALID_ARG, "negative option");
@@ -227,6 +227,7 @@ pagedattn_status pagedattn_plan(const int32_t* qo_indptr, const int32_t* kv_page
     return set_err(s, err);
   }
   plan->force_cp_async = (opts && opts->force_cp_async) ? 1 : 0;
+  plan->decode_cuda_cores = (opts && opts->decode_cuda_cores) ? 1 : 0;
   if (workspace) {
     if (reinterpret_cast<uintptr_t>(workspace) % 256) {
       delete plan;
@@ -292,6 +293,7 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
   a.lse = lse;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.force_cp_async = plan->force_cp_async;
+  a.decode_cuda_cores = plan->decode_cuda_cores;
   if (stage_mask & PA_STAGE_PREFILL) {
     e = pa::launch_prefill(a, hp.ps >= 8 ? &plan->map_sw128 : nullptr, &plan->map_q);
     if (e != cudaSuccess) return cuda_err(e, "prefill launch");

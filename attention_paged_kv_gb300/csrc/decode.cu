@@ -76,51 +76,17 @@ __device__ __forceinline__ uint32_t sw_off(int t, int c) {
   return static_cast<uint32_t>((c >> 3) * DecCfg<D>::BLK + t * 128 + (((c & 7) ^ (t & 7)) << 4));
 }
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p,
-                                               const int use_tma) {
+// Producer warp of the decode kernels: streams the item's keys in 64-key
+// stages (K then V, 128-byte-swizzled rows) into kDecStages buffers, by TMA
+// through the page table or, for pages of fewer than 8 slots, by cp.async.
+// On return every copy it issued has landed (or its wait gave up).
+template <typename T, int D>
+__device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const KParams& p, const DecItem& it,
+                                               const ReqEntry& rq, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                                               volatile int32_t* abort_flag, int use_tma, int nstage, int lane) {
   using C = DecCfg<D>;
   constexpr int NKB = C::NKB;
-  constexpr int NCH = D / 8;       // 16-byte chunks per row
-  constexpr int LPT = D / 8;       // PV lanes per key
-  constexpr int TPS = 32 / LPT;    // PV keys per warp step
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* empty = full + kDecStages;
-  uint64_t* pfull = empty + kDecStages;  // [pairs] QK -> PV
-  uint64_t* pempty = pfull + kDecPairs;  // [pairs] PV -> QK
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(pempty + kDecPairs);
-  float2* qs2 = reinterpret_cast<float2*>(smem + C::OFF_Q);  // [G][D/2]
-
-  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const DecItem it = p.dec[blockIdx.x];
-  const ReqEntry rq = p.req[it.req];
-  const int nstage = (it.tok1 - it.tok0 + kDecTile - 1) / kDecTile;
-  const int64_t qrow0 = int64_t(rq.qo_start) * p.Hq + int64_t(it.kv_head) * G;
-
-  if (tid == 0) {
-    for (int i = 0; i < kDecStages; ++i) {
-      mbar_init(&full[i], use_tma ? 1 : 32);
-      mbar_init(&empty[i], 2);
-    }
-    for (int i = 0; i < kDecPairs; ++i) {
-      mbar_init(&pfull[i], 1);
-      mbar_init(&pempty[i], 1);
-    }
-    *abort_flag = 0;
-    mbar_init_fence();
-  }
-  // q for the G heads, pre-scaled into log2 units, as fp32 column pairs
-  for (int idx = tid; idx < G * D / 2; idx += kDecThreads) {
-    const int g = idx / (D / 2), c2 = idx % (D / 2);
-    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) + (qrow0 + g) * D) + c2);
-    qs2[idx] = __fmul2_rn(Elt<T>::to_f2(w), make_float2(p.scale_log2, p.scale_log2));
-  }
-  __syncthreads();
-
-  if (warp == 2 * kDecPairs) {
-    // ---------------------------------------------------------------- producer
+  constexpr int NCH = D / 8;
     if (use_tma && lane == 0) tma_prefetch_desc(&kv_map);
     const int br_shift = min(p.ps_shift, 6);
     const int BR = 1 << br_shift;  // rows per copy: a page, or 64 slots of it
@@ -194,6 +160,53 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode
       }
     }
     __syncwarp();
+}
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p,
+                                               const int use_tma) {
+  using C = DecCfg<D>;
+  constexpr int NKB = C::NKB;
+  constexpr int NCH = D / 8;       // 16-byte chunks per row
+  constexpr int LPT = D / 8;       // PV lanes per key
+  constexpr int TPS = 32 / LPT;    // PV keys per warp step
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + kDecStages;
+  uint64_t* pfull = empty + kDecStages;  // [pairs] QK -> PV
+  uint64_t* pempty = pfull + kDecPairs;  // [pairs] PV -> QK
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(pempty + kDecPairs);
+  float2* qs2 = reinterpret_cast<float2*>(smem + C::OFF_Q);  // [G][D/2]
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const DecItem it = p.dec[blockIdx.x];
+  const ReqEntry rq = p.req[it.req];
+  const int nstage = (it.tok1 - it.tok0 + kDecTile - 1) / kDecTile;
+  const int64_t qrow0 = int64_t(rq.qo_start) * p.Hq + int64_t(it.kv_head) * G;
+
+  if (tid == 0) {
+    for (int i = 0; i < kDecStages; ++i) {
+      mbar_init(&full[i], use_tma ? 1 : 32);
+      mbar_init(&empty[i], 2);
+    }
+    for (int i = 0; i < kDecPairs; ++i) {
+      mbar_init(&pfull[i], 1);
+      mbar_init(&pempty[i], 1);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  // q for the G heads, pre-scaled into log2 units, as fp32 column pairs
+  for (int idx = tid; idx < G * D / 2; idx += kDecThreads) {
+    const int g = idx / (D / 2), c2 = idx % (D / 2);
+    const uint32_t w = __ldg(reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) + (qrow0 + g) * D) + c2);
+    qs2[idx] = __fmul2_rn(Elt<T>::to_f2(w), make_float2(p.scale_log2, p.scale_log2));
+  }
+  __syncthreads();
+
+  if (warp == 2 * kDecPairs) {
+    decode_produce<T, D>(kv_map, p, it, rq, smem, full, empty, abort_flag, use_tma, nstage, lane);
     asm volatile("bar.arrive 1, %0;" ::"n"(kDecThreads) : "memory");
     return;
   }
@@ -392,6 +405,247 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode
   }
 }
 
+// ---------------------------------------------------------------------------
+// Decode on the tensor cores (warp-level MMA, m16n8k16, fp32 accumulate).
+//
+// At G query heads per kv head the CUDA-core kernel above needs 2*G MACs per
+// cached element, which at G >= 2 is more than the FP32 pipe can sustain at
+// HBM speed; the FlashInfer issue "How are prefill and decode kernels
+// different?" makes the same observation (tensor cores win for GQA decode).
+// The G heads of a request's query token are the M rows of one m16n8k16
+// fragment (rows G..15 are zero), so S = q K^T needs no reshaping:
+//   warp 4     the producer of the CUDA-core kernel (64-key stages, 128-byte
+//              swizzled rows, TMA or cp.async).
+//   warps 0-3  warp w takes keys [16w, 16w+16) of each stage: two ldmatrix
+//              x4 per 16 head columns feed S (two 8-key n-tiles); the online
+//              softmax runs on the accumulator fragment (a quad of lanes
+//              holds one head's row), which then becomes the A fragment of
+//              P V directly, and ldmatrix.trans feeds V.  O stays in
+//              registers; the four warps' states are combined at the end.
+// For requests with fewer than 128 keys P is split into hi + lo halves (two
+// MMAs), as in the prefill kernel, so rows that average few keys keep P's
+// rounding out of the output.
+
+template <typename T>
+struct Mma;
+// Only rows 0..7 of A are live: the A registers of rows 8..15 are zero, and
+// the accumulator of those rows is fed zeros and its result dropped, so a
+// lane keeps two accumulator registers per n-tile instead of four.
+template <>
+struct Mma<__nv_bfloat16> {
+  __device__ static __forceinline__ void run(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    float x2, x3;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %10, %10};"
+        : "+f"(d[0]), "+f"(d[1]), "=f"(x2), "=f"(x3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+  }
+};
+template <>
+struct Mma<__half> {
+  __device__ static __forceinline__ void run(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    float x2, x3;
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %10, %10};"
+        : "+f"(d[0]), "+f"(d[1]), "=f"(x2), "=f"(x3)
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+  }
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr)
+               : "memory");
+}
+
+constexpr int kDmThreads = 160;  // 4 MMA warps + 1 producer
+
+template <typename T, int D, int G>
+__global__ void __launch_bounds__(kDmThreads, 2)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p, const int use_tma) {
+  static_assert(G <= 8, "heads of a group must fit the 8 live rows of the fragment");
+  using C = DecCfg<D>;
+  constexpr int NKS = D / 16;  // k-steps of S
+  constexpr int NNT = D / 8;   // n-tiles of O
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
+  uint64_t* empty = full + kDecStages;
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(empty + kDecStages);
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const DecItem it = p.dec[blockIdx.x];
+  const ReqEntry rq = p.req[it.req];
+  const int nstage = (it.tok1 - it.tok0 + kDecTile - 1) / kDecTile;
+  const int64_t qrow0 = int64_t(rq.qo_start) * p.Hq + int64_t(it.kv_head) * G;
+
+  if (tid == 0) {
+    for (int i = 0; i < kDecStages; ++i) {
+      mbar_init(&full[i], use_tma ? 1 : 32);
+      mbar_init(&empty[i], 4);
+    }
+    *abort_flag = 0;
+    mbar_init_fence();
+  }
+  __syncthreads();
+
+  if (warp == 4) {
+    decode_produce<T, D>(kv_map, p, it, rq, smem, full, empty, abort_flag, use_tma, nstage, lane);
+    asm volatile("bar.arrive 1, %0;" ::"n"(kDmThreads) : "memory");
+    return;
+  }
+
+  const int g = lane >> 2, t = lane & 3;   // fragment row (head) and column pair
+  const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix and row this lane addresses
+  // q as A fragments: row g = head g of the group (zero past G), 16 columns per k-step
+  uint32_t qa0[NKS], qa2[NKS];
+  {
+    const uint32_t* qp = reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) + (qrow0 + g) * D);
+#pragma unroll
+    for (int kk = 0; kk < NKS; ++kk) {
+      qa0[kk] = (g < G) ? __ldg(qp + kk * 8 + t) : 0u;
+      qa2[kk] = (g < G) ? __ldg(qp + kk * 8 + 4 + t) : 0u;
+    }
+  }
+  float o[NNT][2];  // row g (head g), columns 8n + 2t, 8n + 2t + 1
+#pragma unroll
+  for (int n = 0; n < NNT; ++n) o[n][0] = o[n][1] = 0.f;
+  float m_run = -INFINITY, l_part = 0.f;   // row g; l_part sums this lane's columns only
+  const bool split_p = rq.kv_len < 128;
+  const float sl2 = p.scale_log2;
+  const int wt0 = warp * 16;
+
+  for (int j = 0; j < nstage; ++j) {
+    const int st = j % kDecStages;
+    const bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status);
+    if (!__all_sync(0xffffffffu, ok)) break;
+    const int nval = min(kDecTile, it.tok1 - (it.tok0 + j * kDecTile));
+    const uint32_t kbase = smem_u32(smem) + st * C::STAGE;
+    const uint32_t vbase = kbase + C::STAGE_K;
+    if (nval < wt0 + 16) {
+      // keys past the end of the range: zero this warp's V rows (they may
+      // hold anything, and 0 * NaN would poison O); cp.async zero-filled them
+      for (int kr = max(nval - wt0, 0) + (lane >> 3); kr < 16; kr += 4) {
+        uint8_t* vrow = smem + st * C::STAGE + C::STAGE_K + (wt0 + kr) * 128;
+        for (int c = lane & 7; c < 8 * C::NKB; c += 8)
+          *reinterpret_cast<uint4*>(vrow + (c >> 3) * C::BLK + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
+      }
+      __syncwarp();
+    }
+
+    // S = q K^T for keys wt0 .. wt0+15 (n-tiles of 8 keys)
+    float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+#pragma unroll
+    for (int kk = 0; kk < NKS; ++kk) {
+      uint32_t b00, b01, b10, b11;
+      ldsm_x4(kbase + sw_off<D>(wt0 + (mi >> 1) * 8 + ri, 2 * kk + (mi & 1)), b00, b01, b10, b11);
+      Mma<T>::run(sc[0], qa0[kk], qa2[kk], b00, b01);
+      Mma<T>::run(sc[1], qa0[kk], qa2[kk], b10, b11);
+    }
+
+    // online softmax on the fragment: lane holds keys 2t, 2t+1 of each n-tile
+    float sv[4];
+#pragma unroll
+    for (int n = 0; n < 2; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int key = wt0 + n * 8 + 2 * t + e;
+        sv[2 * n + e] = (key < nval) ? sc[n][e] * sl2 : -INFINITY;
+      }
+    float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float m_new = fmaxf(m_run, mx);
+    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
+    const float alpha = ex2f(m_run - m_use);
+    float pv[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) pv[e] = ex2f(sv[e] - m_use);
+    l_part = l_part * alpha + ((pv[0] + pv[1]) + (pv[2] + pv[3]));
+    m_run = m_new;
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+      for (int n = 0; n < NNT; ++n) {
+        o[n][0] *= alpha;
+        o[n][1] *= alpha;
+      }
+    }
+    const uint32_t pa0 = Elt<T>::from_f2(pv[0], pv[1]);
+    const uint32_t pa2 = Elt<T>::from_f2(pv[2], pv[3]);
+    uint32_t la0 = 0u, la2 = 0u;
+    if (split_p) {
+      const float2 h0 = Elt<T>::to_f2(pa0), h2 = Elt<T>::to_f2(pa2);
+      la0 = Elt<T>::from_f2(pv[0] - h0.x, pv[1] - h0.y);
+      la2 = Elt<T>::from_f2(pv[2] - h2.x, pv[3] - h2.y);
+    }
+
+    // O += P V over the 16 keys (pairs of 8-column n-tiles)
+#pragma unroll
+    for (int dp = 0; dp < NNT / 2; ++dp) {
+      uint32_t v0, v1, v2, v3;
+      ldsm_x4_t(vbase + sw_off<D>(wt0 + (mi & 1) * 8 + ri, 2 * dp + (mi >> 1)), v0, v1, v2, v3);
+      Mma<T>::run(o[2 * dp], pa0, pa2, v0, v1);
+      Mma<T>::run(o[2 * dp + 1], pa0, pa2, v2, v3);
+      if (split_p) {
+        Mma<T>::run(o[2 * dp], la0, la2, v0, v1);
+        Mma<T>::run(o[2 * dp + 1], la0, la2, v2, v3);
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(&empty[st]);
+  }
+
+  // ---------------------------------------------------------------- combine the four warps
+  l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
+  l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
+  asm volatile("bar.sync 1, %0;" ::"n"(kDmThreads) : "memory");
+  float* comb_o = reinterpret_cast<float*>(smem);  // [4][G][D], reuses stage memory
+  float* comb_m = comb_o + 4 * G * D;              // [4][G]
+  float* comb_l = comb_m + 4 * G;                  // [4][G]
+  if (g < G) {
+#pragma unroll
+    for (int n = 0; n < NNT; ++n)
+      *reinterpret_cast<float2*>(&comb_o[(warp * G + g) * D + n * 8 + 2 * t]) = make_float2(o[n][0], o[n][1]);
+    if (t == 0) {
+      comb_m[warp * G + g] = m_run;
+      comb_l[warp * G + g] = l_part;
+    }
+  }
+  asm volatile("bar.sync 2, 128;" ::: "memory");
+  if (*abort_flag) return;
+  const bool partial = it.part_row >= 0;
+  for (int idx = tid; idx < G * D; idx += 128) {
+    const int gg = idx / D, d = idx % D;
+    float M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) M = fmaxf(M, comb_m[w * G + gg]);
+    const float Mu = (M == -INFINITY) ? 0.f : M;
+    float L = 0.f, O = 0.f;
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float wq = ex2f(comb_m[w * G + gg] - Mu);
+      L += wq * comb_l[w * G + gg];
+      O += wq * comb_o[(w * G + gg) * D + d];
+    }
+    const float val = L > 0.f ? O / L : 0.f;
+    const float lse = L > 0.f ? (Mu + __log2f(L)) * kLn2f : -INFINITY;
+    if (!partial) {
+      static_cast<T*>(p.out)[(qrow0 + gg) * D + d] = Elt<T>::from_f(val);
+      if (d == 0 && p.lse) p.lse[qrow0 + gg] = lse;
+    } else {
+      p.part_o[(int64_t(it.part_row) + gg) * D + d] = val;
+      if (d == 0) p.part_lse[it.part_row + gg] = lse;
+    }
+  }
+}
+
 // Split-KV merge: one warp per (query token, query head) row of a split
 // group.  Each split s holds o_s (already divided by its own softmax sum)
 // and lse_s = ln(its sum); the whole sum is sum_s exp(lse_s), so
@@ -449,19 +703,32 @@ __global__ void debug_gather_kernel(const KParams p, const int B, int32_t* page_
   }
 }
 
+// Groups of 4 or 8 query heads decode on the warp-MMA kernel unless the
+// plan asks for the CUDA-core one; smaller groups always use CUDA cores
+// (at G <= 2 their FP32 work fits under the HBM time).
 template <typename T, int D, int G>
 cudaError_t launch_decode_t(const RunArgs& a, const CUtensorMap* map, const KParams& kp) {
   using C = DecCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+  const bool mma = G >= 4 && !a.decode_cuda_cores;
+  static bool attr_set[2] = {false, false};
+  if (!attr_set[mma]) {
+    cudaError_t e = mma ? cudaFuncSetAttribute(decode_mma_kernel<T, D, (G >= 4 ? G : 4)>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM)
+                        : cudaFuncSetAttribute(decode_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               C::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[mma] = true;
   }
   const int use_tma = (map != nullptr && a.hp->ps >= 8) ? 1 : 0;
   CUtensorMap dummy;
   if (!use_tma) memset(&dummy, 0, sizeof(dummy));
-  decode_kernel<T, D, G><<<a.hp->n_dec, kDecThreads, C::SMEM, a.stream>>>(use_tma ? *map : dummy, kp, use_tma);
+  if (mma) {
+    if constexpr (G >= 4)
+      decode_mma_kernel<T, D, G><<<a.hp->n_dec, kDmThreads, C::SMEM, a.stream>>>(use_tma ? *map : dummy, kp,
+                                                                                  use_tma);
+  } else {
+    decode_kernel<T, D, G><<<a.hp->n_dec, kDecThreads, C::SMEM, a.stream>>>(use_tma ? *map : dummy, kp, use_tma);
+  }
   return cudaGetLastError();
 }
 

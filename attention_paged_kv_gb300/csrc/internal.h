@@ -46,6 +46,7 @@ struct RunArgs {
   float* lse;
   cudaStream_t stream;
   int force_cp_async;
+  int decode_cuda_cores;  // 1: G in {4, 8} decodes on the CUDA-core kernel
 };
 
 cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const CUtensorMap* map_q);
@@ -72,6 +73,7 @@ struct pagedattn_plan_s {
   size_t workspace_bytes = 0;
   int device = -1;
   int force_cp_async = 0;
+  int decode_cuda_cores = 0;
   // tensor maps over the last kv_cache pointer seen by run()
   const void* map_kv = nullptr;
   CUtensorMap map_rows;   // decode: box {64, 1, min(ps, 64), 1}, 128-byte swizzle (page_size >= 8)

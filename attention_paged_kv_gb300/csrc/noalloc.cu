@@ -97,6 +97,7 @@ extern "C" pagedattn_status pagedattn_run_decode_noalloc(pagedattn_plan_t plan, 
   a.out = out;
   a.lse = lse;
   a.stream = st;
+  a.decode_cuda_cores = plan->decode_cuda_cores;
   e = launch_decode(a, hp.ps >= 8 ? &map : nullptr);
   if (e != cudaSuccess) return cuda_err(e, "no-alloc decode launch");
   e = launch_merge(a);

@@ -354,7 +354,9 @@ def main():
     prefill_obj = {"kernel": "prefill_kernel", "ms": t_pre, "tflops": pre_tflops,
                    "frac_of_bf16_peak": pre_tflops / p_tc, "flops": acc["prefill"]["flops"],
                    "bytes": acc["prefill"]["bytes"]}
-    decode_obj = {"kernel": "decode_kernel+merge_kernel", "ms": dec_time, "decode_ms": t_dec, "merge_ms": t_mrg,
+    G = w.num_qo_heads // w.num_kv_heads
+    dec_name = "decode_mma_kernel" if G in (4, 8) else "decode_kernel"
+    decode_obj = {"kernel": f"{dec_name}+merge_kernel", "ms": dec_time, "decode_ms": t_dec, "merge_ms": t_mrg,
                   "kv_gbs": dec_gbs, "all_bytes_gbs": dec_all_gbs, "frac_of_hbm": dec_all_gbs / peaks["hbm_gbs"],
                   "kv_bytes": acc["decode"]["kv_bytes"], "bytes": acc["decode"]["bytes"]}
     if acc["prefill"]["flops"] and (t_pre >= dec_time or not acc["decode"]["flops"]):
@@ -363,8 +365,8 @@ def main():
                 "unit": "TFLOP/s", "frac": pre_tflops / p_tc, "traffic": traffic,
                 "peak_source": f"{peak_src} {'sustained' if long_run else 'burst'} bf16"}
     else:
-        traffic = profile_traffic("decode_kernel")
-        roof = {"bound": "hbm", "kernel": "decode_kernel+merge_kernel", "achieved": dec_all_gbs,
+        traffic = profile_traffic(dec_name)
+        roof = {"bound": "hbm", "kernel": f"{dec_name}+merge_kernel", "achieved": dec_all_gbs,
                 "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": dec_all_gbs / peaks["hbm_gbs"],
                 "traffic": traffic, "peak_source": f"{peak_src} copy bandwidth"}
 

@@ -81,7 +81,9 @@ typedef struct {
   int32_t decode_chunk_pages;  /* > 0: pages per decode split (default: see plan)    */
   int32_t prefill_chunk_tiles; /* > 0: 128-key tiles per prefill split               */
   int32_t force_cp_async;      /* 1: stage prefill K/V with cp.async instead of TMA   */
-  int32_t reserved[3];         /* must be 0                                          */
+  int32_t decode_cuda_cores;   /* 1: decode groups of 4 or 8 query heads per kv head
+                                  on the CUDA-core kernel (default: warp-level MMA)  */
+  int32_t reserved[2];         /* must be 0                                          */
 } pagedattn_options;
 
 /* Stage bits for pagedattn_run_stages. */

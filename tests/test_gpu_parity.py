@@ -1,6 +1,8 @@
 """GPU parity: the CUDA path, called through the C ABI, against the fp64
 oracle on the same seeded inputs, plus the invariants that must hold
 bit-exactly on the GPU (page placement, prefix sharing) and edge cases."""
+import dataclasses
+
 import numpy as np
 import pytest
 import torch
@@ -34,7 +36,8 @@ def test_tiny_all_paths(opts):
     assert_close(out, lse, ro, rl, w.dtype, what=f"tiny {opts}")
 
 
-@pytest.mark.parametrize("opts", [{}, {"decode_chunk_pages": 64}, {"decode_chunk_pages": 1}])
+@pytest.mark.parametrize("opts", [{}, {"decode_chunk_pages": 64}, {"decode_chunk_pages": 1},
+                                  {"decode_cuda_cores": True}, {"decode_cuda_cores": True, "decode_chunk_pages": 1}])
 def test_decode_script_batch(opts):
     w = workloads.decode()
     ro, rl = A.attention(w)
@@ -42,14 +45,40 @@ def test_decode_script_batch(opts):
     assert_close(out, lse, ro, rl, w.dtype, what=f"decode {opts}")
 
 
-def test_decode_equals_prefill_qo1():
+@pytest.mark.parametrize("cuda_cores", [False, True])
+def test_decode_equals_prefill_qo1(cuda_cores):
     """The timing script's closing check: decode output allclose to the
     prefill kernel's output on the same qo_len = 1 batch (atol = rtol = 1e-3)."""
     w = workloads.decode()
-    o_dec, l_dec, _ = run(w)
+    o_dec, l_dec, _ = run(w, decode_cuda_cores=cuda_cores)
     o_pre, l_pre, _ = run(w, force_prefill=True)
     assert np.allclose(o_dec, o_pre, atol=1e-3, rtol=1e-3)
     assert np.allclose(l_dec, l_pre, atol=1e-3, rtol=1e-3)
+
+
+@pytest.mark.parametrize("opts", [{}, {"decode_cuda_cores": True}, {"force_prefill": True},
+                                  {"force_cp_async": True, "force_prefill": True}])
+@pytest.mark.parametrize("ps", [4, 16, 128])
+def test_nan_outside_the_kv_range(opts, ps):
+    """Slots past each request's last_page_len and pages no request uses
+    hold NaN: no kernel may let them reach an output (masked keys still
+    meet V in the P V product, where 0 * NaN would be NaN)."""
+    lens = [1, 63, 64, 65, 127, 129, 200, 1000, 100, 300]
+    qo = [1] * 8 + [40, 130]
+    w = workloads.make_custom("nan", qo, lens, 16, 2, 128, ps, dtype=torch.bfloat16, seed=ps + 3, extra_pages=5)
+    used = torch.zeros(w.num_pages, dtype=torch.bool)
+    kv = w.kv_cache.clone()
+    for b in range(len(lens)):
+        pages = torch.as_tensor(np.asarray(w.kv_page_indices[w.kv_page_indptr[b]:w.kv_page_indptr[b + 1]]),
+                                dtype=torch.long)
+        used[pages] = True
+        kv[int(pages[-1]), :, int(w.kv_last_page_len[b]):] = float("nan")
+    kv[~used] = float("nan")
+    w = dataclasses.replace(w, kv_cache=kv)
+    ro, rl = A.attention(w)
+    assert np.isfinite(ro).all()
+    out, lse, _ = run(w, **opts)
+    assert_close(out, lse, ro, rl, w.dtype, what=f"NaN outside range {opts} ps {ps}")
 
 
 def test_ragged_prefill():
@@ -172,11 +201,14 @@ def test_device_metadata_equals_restated_plan():
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
 def test_shapes_groups_dtypes(dtype, D, G):
     Hkv = 2
-    w = workloads.make_custom("s", [1, 7, 1, 33, 0, 140], [1, 7, 300, 200, 5, 333], G * Hkv, Hkv, D, 16,
+    w = workloads.make_custom("s", [1, 7, 1, 33, 0, 140, 1], [1, 7, 300, 200, 5, 333, 64], G * Hkv, Hkv, D, 16,
                               dtype=dtype, seed=G * 100 + D)
     ro, rl = A.attention(w)
     out, lse, _ = run(w)
     assert_close(out, lse, ro, rl, dtype, what=f"D{D} G{G} {dtype}")
+    if G in (4, 8):  # the same batch on the CUDA-core decode kernel
+        out, lse, _ = run(w, decode_cuda_cores=True)
+        assert_close(out, lse, ro, rl, dtype, what=f"D{D} G{G} {dtype} CUDA-core decode")
 
 
 @pytest.mark.parametrize("ps", [1, 2, 8, 32, 64, 128])
