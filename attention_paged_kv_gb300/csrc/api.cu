@@ -127,6 +127,7 @@ pagedattn_status fill_inputs(pa::PlanInputs* in, const int32_t* qo_indptr, const
   in->force_prefill = o.force_prefill ? 1 : 0;
   in->decode_chunk_pages = o.decode_chunk_pages;
   in->prefill_chunk_tiles = o.prefill_chunk_tiles;
+  in->decode_cuda_cores = o.decode_cuda_cores ? 1 : 0;
   if (in->num_sms == 0) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -227,7 +228,6 @@ pagedattn_status pagedattn_plan(const int32_t* qo_indptr, const int32_t* kv_page
     return set_err(s, err);
   }
   plan->force_cp_async = (opts && opts->force_cp_async) ? 1 : 0;
-  plan->decode_cuda_cores = (opts && opts->decode_cuda_cores) ? 1 : 0;
   if (workspace) {
     if (reinterpret_cast<uintptr_t>(workspace) % 256) {
       delete plan;
@@ -293,7 +293,6 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
   a.lse = lse;
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.force_cp_async = plan->force_cp_async;
-  a.decode_cuda_cores = plan->decode_cuda_cores;
   if (stage_mask & PA_STAGE_PREFILL) {
     e = pa::launch_prefill(a, hp.ps >= 8 ? &plan->map_sw128 : nullptr, &plan->map_q);
     if (e != cudaSuccess) return cuda_err(e, "prefill launch");

@@ -406,51 +406,72 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode
 }
 
 // ---------------------------------------------------------------------------
-// Decode on the tensor cores (warp-level MMA, m16n8k16, fp32 accumulate).
+// Small-query kernel on the tensor cores (warp-level MMA, m16n8k16, fp32
+// accumulate): decode, and requests of a few query tokens (speculative
+// decoding, small chunks) whose qo_len * G packed (token, head) rows number
+// at most 64.
 //
 // At G query heads per kv head the CUDA-core kernel above needs 2*G MACs per
-// cached element, which at G >= 2 is more than the FP32 pipe can sustain at
-// HBM speed; the FlashInfer issue "How are prefill and decode kernels
-// different?" makes the same observation (tensor cores win for GQA decode).
-// The G heads of a request's query token are the M rows of one m16n8k16
-// fragment (rows G..15 are zero), so S = q K^T needs no reshaping:
+// cached element, more than the FP32 pipe sustains at HBM speed once G >= 4;
+// the FlashInfer issue "How are prefill and decode kernels different?" makes
+// the same point (tensor cores pay off for grouped-query decode) and names a
+// small-query variant of the prefill kernel as missing.  Here the packed rows
+// r = token * G + head of an item are the M rows of m16n8k16 fragments, so
+// S = q K^T needs no reshaping:
 //   warp 4     the producer of the CUDA-core kernel (64-key stages, 128-byte
 //              swizzled rows, TMA or cp.async).
-//   warps 0-3  warp w takes keys [16w, 16w+16) of each stage: two ldmatrix
-//              x4 per 16 head columns feed S (two 8-key n-tiles); the online
-//              softmax runs on the accumulator fragment (a quad of lanes
-//              holds one head's row), which then becomes the A fragment of
-//              P V directly, and ldmatrix.trans feeds V.  O stays in
-//              registers; the four warps' states are combined at the end.
-// For requests with fewer than 128 keys P is split into hi + lo halves (two
-// MMAs), as in the prefill kernel, so rows that average few keys keep P's
-// rounding out of the output.
+//   warps 0-3  row group rg = warp % RGN (16 rows each), key subset
+//              kq = warp / RGN of every stage: with RGN row groups each warp
+//              takes 16 * RGN of the stage's 64 keys.  ldmatrix feeds K from
+//              the swizzled rows; the online softmax runs on the accumulator
+//              fragment (a quad of lanes holds a row), whose exp2 values
+//              become the A fragment of P V directly; ldmatrix.trans feeds V.
+//              O stays in registers; the key subsets are combined at the end.
+// Row classes (template RC): 8 rows (RGN 1; the accumulators of the unused
+// rows 8..15 are fed zeros and dropped), 16 rows (RGN 1), 32 (RGN 2) and 64
+// (RGN 4).  Each row's keys end at its own causal limit.  For requests with
+// fewer than 128 keys P is split into hi + lo halves (two MMAs), as in the
+// prefill kernel, so rows that see few keys keep P's rounding out of the
+// output.
 
 template <typename T>
-struct Mma;
-// Only rows 0..7 of A are live: the A registers of rows 8..15 are zero, and
-// the accumulator of those rows is fed zeros and its result dropped, so a
-// lane keeps two accumulator registers per n-tile instead of four.
-template <>
-struct Mma<__nv_bfloat16> {
-  __device__ static __forceinline__ void run(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+struct Mma {
+  // rows 0..7 only: the A registers of rows 8..15 are zero and their
+  // accumulators are fed zeros and dropped (two registers per n-tile)
+  __device__ static __forceinline__ void half(float (&d)[2], const uint32_t (&a)[2], uint32_t b0, uint32_t b1) {
     float x2, x3;
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %10, %10};"
-        : "+f"(d[0]), "+f"(d[1]), "=f"(x2), "=f"(x3)
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+    if constexpr (Elt<T>::kBf16)
+      asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+          "{%0, %1, %10, %10};"
+          : "+f"(d[0]), "+f"(d[1]), "=f"(x2), "=f"(x3)
+          : "r"(a[0]), "r"(0u), "r"(a[1]), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+    else
+      asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+          "{%0, %1, %10, %10};"
+          : "+f"(d[0]), "+f"(d[1]), "=f"(x2), "=f"(x3)
+          : "r"(a[0]), "r"(0u), "r"(a[1]), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
+  }
+  // all 16 rows; a = {row g cols 2t.., row g cols 2t+8.., row g+8 cols 2t.., row g+8 cols 2t+8..}
+  __device__ static __forceinline__ void full(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+    if constexpr (Elt<T>::kBf16)
+      asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+          "{%0, %1, %2, %3};"
+          : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+          : "r"(a[0]), "r"(a[2]), "r"(a[1]), "r"(a[3]), "r"(b0), "r"(b1));
+    else
+      asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+          "{%0, %1, %2, %3};"
+          : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+          : "r"(a[0]), "r"(a[2]), "r"(a[1]), "r"(a[3]), "r"(b0), "r"(b1));
   }
 };
-template <>
-struct Mma<__half> {
-  __device__ static __forceinline__ void run(float (&d)[2], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-    float x2, x3;
-    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-        "{%0, %1, %10, %10};"
-        : "+f"(d[0]), "+f"(d[1]), "=f"(x2), "=f"(x3)
-        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
-  }
-};
+template <typename T, int NA>
+__device__ __forceinline__ void mma_rows(float (&d)[NA], const uint32_t (&a)[NA], uint32_t b0, uint32_t b1) {
+  if constexpr (NA == 2)
+    Mma<T>::half(d, a, b0, b1);
+  else
+    Mma<T>::full(d, a, b0, b1);
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
@@ -467,11 +488,23 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
 
 constexpr int kDmThreads = 160;  // 4 MMA warps + 1 producer
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kDmThreads, 2)
-    decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p, const int use_tma) {
-  static_assert(G <= 8, "heads of a group must fit the 8 live rows of the fragment");
+template <int RC>
+struct RowClass {
+  static constexpr bool HALF = RC == 0;                        // rows 8..15 unused
+  static constexpr int RGN = RC <= 1 ? 1 : (RC == 2 ? 2 : 4);  // row groups of 16
+  static constexpr int KS = 4 / RGN;                           // key subsets (warps per row group)
+  static constexpr int KW = kDecTile / KS;                     // keys per warp per stage
+  static constexpr int NKB = KW / 16;                          // 16-key blocks per warp
+  static constexpr int NA = HALF ? 2 : 4;                      // accumulator registers per n-tile
+};
+
+template <typename T, int D, int RC>
+__global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
+    decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p, const int use_tma,
+                      const int item0) {
   using C = DecCfg<D>;
+  using RCl = RowClass<RC>;
+  constexpr int RGN = RCl::RGN, KS = RCl::KS, KW = RCl::KW, NKB = RCl::NKB, NA = RCl::NA;
   constexpr int NKS = D / 16;  // k-steps of S
   constexpr int NNT = D / 8;   // n-tiles of O
   extern __shared__ uint8_t smem_raw[];
@@ -481,10 +514,10 @@ __global__ void __launch_bounds__(kDmThreads, 2)
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(empty + kDecStages);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const DecItem it = p.dec[blockIdx.x];
+  const DecItem it = p.dec[item0 + blockIdx.x];
   const ReqEntry rq = p.req[it.req];
   const int nstage = (it.tok1 - it.tok0 + kDecTile - 1) / kDecTile;
-  const int64_t qrow0 = int64_t(rq.qo_start) * p.Hq + int64_t(it.kv_head) * G;
+  const int R = rq.qo_len << p.g_shift;  // packed rows: r = token * G + head
 
   if (tid == 0) {
     for (int i = 0; i < kDecStages; ++i) {
@@ -502,146 +535,244 @@ __global__ void __launch_bounds__(kDmThreads, 2)
     return;
   }
 
-  const int g = lane >> 2, t = lane & 3;   // fragment row (head) and column pair
+  const int rg = warp % RGN, kq = warp / RGN;
+  const int g = lane >> 2, t = lane & 3;    // fragment row and column pair
   const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix and row this lane addresses
-  // q as A fragments: row g = head g of the group (zero past G), 16 columns per k-step
-  uint32_t qa0[NKS], qa2[NKS];
+  const int r_lo = rg * 16 + g, r_hi = r_lo + 8;
+  // global q / out row of packed row r
+  auto row_of = [&](int r) -> int64_t {
+    return int64_t(rq.qo_start + (r >> p.g_shift)) * p.Hq + int64_t(it.kv_head) * p.G + (r & (p.G - 1));
+  };
+  // end (exclusive, absolute key position) of the keys row r may see in this item:
+  // the item's range, cut at the row's bottom-right causal limit
+  auto end_of = [&](int r) -> int {
+    if (r >= R) return 0;
+    const int lim = p.causal ? rq.kv_len - rq.qo_len + (r >> p.g_shift) + 1 : rq.kv_len;
+    return min(it.tok1, lim);
+  };
+  const int end_lo = end_of(r_lo), end_hi = RCl::HALF ? 0 : end_of(r_hi);
+
+  // q as A fragments: {row lo cols 2t, row lo cols 2t+8, row hi cols 2t, row hi cols 2t+8} per k-step
+  uint32_t qa[NKS][NA];
   {
-    const uint32_t* qp = reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) + (qrow0 + g) * D);
+    const T* q = static_cast<const T*>(p.q);
 #pragma unroll
-    for (int kk = 0; kk < NKS; ++kk) {
-      qa0[kk] = (g < G) ? __ldg(qp + kk * 8 + t) : 0u;
-      qa2[kk] = (g < G) ? __ldg(qp + kk * 8 + 4 + t) : 0u;
+    for (int kk = 0; kk < NKS; ++kk) qa[kk][0] = qa[kk][1] = 0u;
+    if (r_lo < R) {
+      const uint32_t* qp = reinterpret_cast<const uint32_t*>(q + row_of(r_lo) * D);
+#pragma unroll
+      for (int kk = 0; kk < NKS; ++kk) {
+        qa[kk][0] = __ldg(qp + kk * 8 + t);
+        qa[kk][1] = __ldg(qp + kk * 8 + 4 + t);
+      }
+    }
+    if constexpr (NA == 4) {
+#pragma unroll
+      for (int kk = 0; kk < NKS; ++kk) qa[kk][2] = qa[kk][3] = 0u;
+      if (r_hi < R) {
+        const uint32_t* qp = reinterpret_cast<const uint32_t*>(q + row_of(r_hi) * D);
+#pragma unroll
+        for (int kk = 0; kk < NKS; ++kk) {
+          qa[kk][2] = __ldg(qp + kk * 8 + t);
+          qa[kk][3] = __ldg(qp + kk * 8 + 4 + t);
+        }
+      }
     }
   }
-  float o[NNT][2];  // row g (head g), columns 8n + 2t, 8n + 2t + 1
+  float o[NNT][NA];  // rows lo (regs 0, 1) and hi (2, 3); columns 8n + 2t, 8n + 2t + 1
 #pragma unroll
-  for (int n = 0; n < NNT; ++n) o[n][0] = o[n][1] = 0.f;
-  float m_run = -INFINITY, l_part = 0.f;   // row g; l_part sums this lane's columns only
+  for (int n = 0; n < NNT; ++n)
+#pragma unroll
+    for (int e = 0; e < NA; ++e) o[n][e] = 0.f;
+  float m_lo = -INFINITY, m_hi = -INFINITY;
+  float l_lo = 0.f, l_hi = 0.f;  // sums over this lane's columns only
   const bool split_p = rq.kv_len < 128;
   const float sl2 = p.scale_log2;
-  const int wt0 = warp * 16;
+  const int kofs = kq * KW;  // this warp's first key in every stage
 
   for (int j = 0; j < nstage; ++j) {
     const int st = j % kDecStages;
     const bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status);
     if (!__all_sync(0xffffffffu, ok)) break;
-    const int nval = min(kDecTile, it.tok1 - (it.tok0 + j * kDecTile));
+    const int s0 = it.tok0 + j * kDecTile;         // absolute position of the stage's first key
+    const int nval = min(kDecTile, it.tok1 - s0);  // keys of the stage inside the item's range
     const uint32_t kbase = smem_u32(smem) + st * C::STAGE;
     const uint32_t vbase = kbase + C::STAGE_K;
-    if (nval < wt0 + 16) {
-      // keys past the end of the range: zero this warp's V rows (they may
-      // hold anything, and 0 * NaN would poison O); cp.async zero-filled them
-      for (int kr = max(nval - wt0, 0) + (lane >> 3); kr < 16; kr += 4) {
-        uint8_t* vrow = smem + st * C::STAGE + C::STAGE_K + (wt0 + kr) * 128;
-        for (int c = lane & 7; c < 8 * C::NKB; c += 8)
-          *reinterpret_cast<uint4*>(vrow + (c >> 3) * C::BLK + (c & 7) * 16) = make_uint4(0, 0, 0, 0);
-      }
-      __syncwarp();
-    }
 
-    // S = q K^T for keys wt0 .. wt0+15 (n-tiles of 8 keys)
-    float sc[2][2] = {{0.f, 0.f}, {0.f, 0.f}};
+    // S = q K^T for keys kofs .. kofs + KW - 1 of the stage (n-tiles of 8 keys)
+    float sc[2 * NKB][NA];
+#pragma unroll
+    for (int n = 0; n < 2 * NKB; ++n)
+#pragma unroll
+      for (int e = 0; e < NA; ++e) sc[n][e] = 0.f;
 #pragma unroll
     for (int kk = 0; kk < NKS; ++kk) {
-      uint32_t b00, b01, b10, b11;
-      ldsm_x4(kbase + sw_off<D>(wt0 + (mi >> 1) * 8 + ri, 2 * kk + (mi & 1)), b00, b01, b10, b11);
-      Mma<T>::run(sc[0], qa0[kk], qa2[kk], b00, b01);
-      Mma<T>::run(sc[1], qa0[kk], qa2[kk], b10, b11);
+#pragma unroll
+      for (int kb = 0; kb < NKB; ++kb) {
+        uint32_t b00, b01, b10, b11;
+        ldsm_x4(kbase + sw_off<D>(kofs + kb * 16 + (mi >> 1) * 8 + ri, 2 * kk + (mi & 1)), b00, b01, b10, b11);
+        mma_rows<T, NA>(sc[2 * kb], qa[kk], b00, b01);
+        mma_rows<T, NA>(sc[2 * kb + 1], qa[kk], b10, b11);
+      }
     }
 
-    // online softmax on the fragment: lane holds keys 2t, 2t+1 of each n-tile
-    float sv[4];
+    // online softmax on the fragment: this lane holds keys 8n + 2t + e of rows lo and hi
+    float mx_lo = -INFINITY, mx_hi = -INFINITY;
 #pragma unroll
-    for (int n = 0; n < 2; ++n)
+    for (int n = 0; n < 2 * NKB; ++n)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int key = wt0 + n * 8 + 2 * t + e;
-        sv[2 * n + e] = (key < nval) ? sc[n][e] * sl2 : -INFINITY;
+        const int key = s0 + kofs + n * 8 + 2 * t + e;
+        sc[n][e] = key < end_lo ? sc[n][e] * sl2 : -INFINITY;
+        mx_lo = fmaxf(mx_lo, sc[n][e]);
+        if constexpr (NA == 4) {
+          sc[n][2 + e] = key < end_hi ? sc[n][2 + e] * sl2 : -INFINITY;
+          mx_hi = fmaxf(mx_hi, sc[n][2 + e]);
+        }
       }
-    float mx = fmaxf(fmaxf(sv[0], sv[1]), fmaxf(sv[2], sv[3]));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    const float m_new = fmaxf(m_run, mx);
-    const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-    const float alpha = ex2f(m_run - m_use);
-    float pv[4];
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+    const float mn_lo = fmaxf(m_lo, mx_lo);
+    const float mu_lo = (mn_lo == -INFINITY) ? 0.f : mn_lo;
+    const float al_lo = ex2f(m_lo - mu_lo);
+    m_lo = mn_lo;
+    float mu_hi = 0.f, al_hi = 1.f;
+    if constexpr (NA == 4) {
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      const float mn_hi = fmaxf(m_hi, mx_hi);
+      mu_hi = (mn_hi == -INFINITY) ? 0.f : mn_hi;
+      al_hi = ex2f(m_hi - mu_hi);
+      m_hi = mn_hi;
+    }
+    float ps_lo = 0.f, ps_hi = 0.f;
 #pragma unroll
-    for (int e = 0; e < 4; ++e) pv[e] = ex2f(sv[e] - m_use);
-    l_part = l_part * alpha + ((pv[0] + pv[1]) + (pv[2] + pv[3]));
-    m_run = m_new;
-    if (__any_sync(0xffffffffu, alpha != 1.f)) {
+    for (int n = 0; n < 2 * NKB; ++n)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        sc[n][e] = ex2f(sc[n][e] - mu_lo);
+        ps_lo += sc[n][e];
+        if constexpr (NA == 4) {
+          sc[n][2 + e] = ex2f(sc[n][2 + e] - mu_hi);
+          ps_hi += sc[n][2 + e];
+        }
+      }
+    l_lo = l_lo * al_lo + ps_lo;
+    l_hi = l_hi * al_hi + ps_hi;
+    if (__any_sync(0xffffffffu, al_lo != 1.f || al_hi != 1.f)) {
 #pragma unroll
       for (int n = 0; n < NNT; ++n) {
-        o[n][0] *= alpha;
-        o[n][1] *= alpha;
+        o[n][0] *= al_lo;
+        o[n][1] *= al_lo;
+        if constexpr (NA == 4) {
+          o[n][2] *= al_hi;
+          o[n][3] *= al_hi;
+        }
       }
     }
-    const uint32_t pa0 = Elt<T>::from_f2(pv[0], pv[1]);
-    const uint32_t pa2 = Elt<T>::from_f2(pv[2], pv[3]);
-    uint32_t la0 = 0u, la2 = 0u;
-    if (split_p) {
-      const float2 h0 = Elt<T>::to_f2(pa0), h2 = Elt<T>::to_f2(pa2);
-      la0 = Elt<T>::from_f2(pv[0] - h0.x, pv[1] - h0.y);
-      la2 = Elt<T>::from_f2(pv[2] - h2.x, pv[3] - h2.y);
-    }
 
-    // O += P V over the 16 keys (pairs of 8-column n-tiles)
+    // P as A fragments of P V, one per 16-key block (n-tiles 2kb, 2kb + 1),
+    // plus the rounding remainder when P is split
+    uint32_t pa[NKB][NA], la[NKB][NA];
 #pragma unroll
-    for (int dp = 0; dp < NNT / 2; ++dp) {
-      uint32_t v0, v1, v2, v3;
-      ldsm_x4_t(vbase + sw_off<D>(wt0 + (mi & 1) * 8 + ri, 2 * dp + (mi >> 1)), v0, v1, v2, v3);
-      Mma<T>::run(o[2 * dp], pa0, pa2, v0, v1);
-      Mma<T>::run(o[2 * dp + 1], pa0, pa2, v2, v3);
-      if (split_p) {
-        Mma<T>::run(o[2 * dp], la0, la2, v0, v1);
-        Mma<T>::run(o[2 * dp + 1], la0, la2, v2, v3);
+    for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+      for (int x = 0; x < NA; ++x) {
+        // x = 0, 1: row lo, keys 2t.. and 8 + 2t..; x = 2, 3: row hi
+        const float v0 = sc[2 * kb + (x & 1)][(x >> 1) * 2];
+        const float v1 = sc[2 * kb + (x & 1)][(x >> 1) * 2 + 1];
+        pa[kb][x] = Elt<T>::from_f2(v0, v1);
+        la[kb][x] = 0u;
+        if (split_p) {
+          const float2 h = Elt<T>::to_f2(pa[kb][x]);
+          la[kb][x] = Elt<T>::from_f2(v0 - h.x, v1 - h.y);
+        }
+      }
+
+    // O += P V; V rows of keys past the range (other data, or stale stage
+    // contents: possibly NaN) are zeroed in the fragments, since 0 * NaN = NaN
+    const bool vpart = nval < kofs + KW;
+#pragma unroll
+    for (int kb = 0; kb < NKB; ++kb) {
+      uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+      if (vpart) {
+        const int k0 = kofs + kb * 16 + 2 * t;  // ldmatrix.trans: this lane's keys 2t, 2t+1 (+8)
+        mlo = (k0 < nval ? 0x0000ffffu : 0u) | (k0 + 1 < nval ? 0xffff0000u : 0u);
+        mhi = (k0 + 8 < nval ? 0x0000ffffu : 0u) | (k0 + 9 < nval ? 0xffff0000u : 0u);
+      }
+#pragma unroll
+      for (int dp = 0; dp < NNT / 2; ++dp) {
+        uint32_t v0, v1, v2, v3;
+        ldsm_x4_t(vbase + sw_off<D>(kofs + kb * 16 + (mi & 1) * 8 + ri, 2 * dp + (mi >> 1)), v0, v1, v2, v3);
+        v0 &= mlo;
+        v1 &= mhi;
+        v2 &= mlo;
+        v3 &= mhi;
+        mma_rows<T, NA>(o[2 * dp], pa[kb], v0, v1);
+        mma_rows<T, NA>(o[2 * dp + 1], pa[kb], v2, v3);
+        if (split_p) {
+          mma_rows<T, NA>(o[2 * dp], la[kb], v0, v1);
+          mma_rows<T, NA>(o[2 * dp + 1], la[kb], v2, v3);
+        }
       }
     }
     __syncwarp();
     if (lane == 0) mbar_arrive(&empty[st]);
   }
 
-  // ---------------------------------------------------------------- combine the four warps
-  l_part += __shfl_xor_sync(0xffffffffu, l_part, 1);
-  l_part += __shfl_xor_sync(0xffffffffu, l_part, 2);
-  asm volatile("bar.sync 1, %0;" ::"n"(kDmThreads) : "memory");
-  float* comb_o = reinterpret_cast<float*>(smem);  // [4][G][D], reuses stage memory
-  float* comb_m = comb_o + 4 * G * D;              // [4][G]
-  float* comb_l = comb_m + 4 * G;                  // [4][G]
-  if (g < G) {
+  // ---------------------------------------------------------------- combine the key subsets
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+  asm volatile("bar.sync 1, %0;" ::"n"(kDmThreads) : "memory");  // stage memory is free from here
+  float* comb_o = reinterpret_cast<float*>(smem);  // [4 warps][16 rows][D]
+  float* comb_m = comb_o + 4 * 16 * D;             // [4][16]
+  float* comb_l = comb_m + 4 * 16;                 // [4][16]
 #pragma unroll
-    for (int n = 0; n < NNT; ++n)
-      *reinterpret_cast<float2*>(&comb_o[(warp * G + g) * D + n * 8 + 2 * t]) = make_float2(o[n][0], o[n][1]);
-    if (t == 0) {
-      comb_m[warp * G + g] = m_run;
-      comb_l[warp * G + g] = l_part;
+  for (int n = 0; n < NNT; ++n) {
+    *reinterpret_cast<float2*>(&comb_o[(warp * 16 + g) * D + n * 8 + 2 * t]) = make_float2(o[n][0], o[n][1]);
+    if constexpr (NA == 4)
+      *reinterpret_cast<float2*>(&comb_o[(warp * 16 + g + 8) * D + n * 8 + 2 * t]) =
+          make_float2(o[n][2], o[n][3]);
+  }
+  if (t == 0) {
+    comb_m[warp * 16 + g] = m_lo;
+    comb_l[warp * 16 + g] = l_lo;
+    if constexpr (NA == 4) {
+      comb_m[warp * 16 + g + 8] = m_hi;
+      comb_l[warp * 16 + g + 8] = l_hi;
     }
   }
   asm volatile("bar.sync 2, 128;" ::: "memory");
   if (*abort_flag) return;
   const bool partial = it.part_row >= 0;
-  for (int idx = tid; idx < G * D; idx += 128) {
-    const int gg = idx / D, d = idx % D;
+  for (int idx = tid; idx < 16 * RGN * D; idx += 128) {
+    const int r = idx / D, d = idx % D;
+    if (r >= R) break;  // rows are visited in increasing order
+    const int rgr = r >> 4, rr = r & 15;
     float M = -INFINITY;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) M = fmaxf(M, comb_m[w * G + gg]);
+    for (int k = 0; k < KS; ++k) M = fmaxf(M, comb_m[(rgr + k * RGN) * 16 + rr]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
     float L = 0.f, O = 0.f;
 #pragma unroll
-    for (int w = 0; w < 4; ++w) {
-      const float wq = ex2f(comb_m[w * G + gg] - Mu);
-      L += wq * comb_l[w * G + gg];
-      O += wq * comb_o[(w * G + gg) * D + d];
+    for (int k = 0; k < KS; ++k) {
+      const int w = rgr + k * RGN;
+      const float wq = ex2f(comb_m[w * 16 + rr] - Mu);
+      L += wq * comb_l[w * 16 + rr];
+      O += wq * comb_o[(w * 16 + rr) * D + d];
     }
     const float val = L > 0.f ? O / L : 0.f;
     const float lse = L > 0.f ? (Mu + __log2f(L)) * kLn2f : -INFINITY;
     if (!partial) {
-      static_cast<T*>(p.out)[(qrow0 + gg) * D + d] = Elt<T>::from_f(val);
-      if (d == 0 && p.lse) p.lse[qrow0 + gg] = lse;
+      const int64_t orow = int64_t(rq.qo_start + (r >> p.g_shift)) * p.Hq + int64_t(it.kv_head) * p.G +
+                           (r & (p.G - 1));
+      static_cast<T*>(p.out)[orow * D + d] = Elt<T>::from_f(val);
+      if (d == 0 && p.lse) p.lse[orow] = lse;
     } else {
-      p.part_o[(int64_t(it.part_row) + gg) * D + d] = val;
-      if (d == 0) p.part_lse[it.part_row + gg] = lse;
+      p.part_o[(int64_t(it.part_row) + r) * D + d] = val;
+      if (d == 0) p.part_lse[it.part_row + r] = lse;
     }
   }
 }
@@ -703,44 +834,68 @@ __global__ void debug_gather_kernel(const KParams p, const int B, int32_t* page_
   }
 }
 
-// Groups of 4 or 8 query heads decode on the warp-MMA kernel unless the
-// plan asks for the CUDA-core one; smaller groups always use CUDA cores
-// (at G <= 2 their FP32 work fits under the HBM time).
 template <typename T, int D, int G>
-cudaError_t launch_decode_t(const RunArgs& a, const CUtensorMap* map, const KParams& kp) {
+cudaError_t launch_cuda_cores(const RunArgs& a, const CUtensorMap* map, const KParams& kp, int use_tma) {
   using C = DecCfg<D>;
-  const bool mma = G >= 4 && !a.decode_cuda_cores;
-  static bool attr_set[2] = {false, false};
-  if (!attr_set[mma]) {
-    cudaError_t e = mma ? cudaFuncSetAttribute(decode_mma_kernel<T, D, (G >= 4 ? G : 4)>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM)
-                        : cudaFuncSetAttribute(decode_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               C::SMEM);
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
-    attr_set[mma] = true;
+    attr_set = true;
   }
-  const int use_tma = (map != nullptr && a.hp->ps >= 8) ? 1 : 0;
-  CUtensorMap dummy;
-  if (!use_tma) memset(&dummy, 0, sizeof(dummy));
-  if (mma) {
-    if constexpr (G >= 4)
-      decode_mma_kernel<T, D, G><<<a.hp->n_dec, kDmThreads, C::SMEM, a.stream>>>(use_tma ? *map : dummy, kp,
-                                                                                  use_tma);
-  } else {
-    decode_kernel<T, D, G><<<a.hp->n_dec, kDecThreads, C::SMEM, a.stream>>>(use_tma ? *map : dummy, kp, use_tma);
-  }
+  decode_kernel<T, D, G><<<a.hp->n_dec, kDecThreads, C::SMEM, a.stream>>>(*map, kp, use_tma);
   return cudaGetLastError();
 }
 
+template <typename T, int D, int RC>
+cudaError_t launch_mma(const RunArgs& a, const CUtensorMap* map, const KParams& kp, int use_tma, int item0,
+                       int n) {
+  using C = DecCfg<D>;
+  static bool attr_set = false;
+  if (!attr_set) {
+    cudaError_t e =
+        cudaFuncSetAttribute(decode_mma_kernel<T, D, RC>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  decode_mma_kernel<T, D, RC><<<n, kDmThreads, C::SMEM, a.stream>>>(*map, kp, use_tma, item0);
+  return cudaGetLastError();
+}
+
+// The plan fixes the kernel: CUDA cores (one launch, every item a single
+// query token at G <= 8), or the warp-MMA kernel with one launch per row
+// class over that class's consecutive items.
 template <typename T, int D>
 cudaError_t launch_decode_d(const RunArgs& a, const CUtensorMap* map, const KParams& kp) {
-  switch (a.hp->G) {
-    case 1: return launch_decode_t<T, D, 1>(a, map, kp);
-    case 2: return launch_decode_t<T, D, 2>(a, map, kp);
-    case 4: return launch_decode_t<T, D, 4>(a, map, kp);
-    case 8: return launch_decode_t<T, D, 8>(a, map, kp);
-    default: return cudaErrorInvalidValue;
+  const HostPlan& hp = *a.hp;
+  const int use_tma = (map != nullptr && hp.ps >= 8) ? 1 : 0;
+  CUtensorMap dummy;
+  memset(&dummy, 0, sizeof(dummy));
+  const CUtensorMap* m = use_tma ? map : &dummy;
+  if (hp.dec_cores) {
+    switch (hp.G) {
+      case 1: return launch_cuda_cores<T, D, 1>(a, m, kp, use_tma);
+      case 2: return launch_cuda_cores<T, D, 2>(a, m, kp, use_tma);
+      case 4: return launch_cuda_cores<T, D, 4>(a, m, kp, use_tma);
+      case 8: return launch_cuda_cores<T, D, 8>(a, m, kp, use_tma);
+      default: return cudaErrorInvalidValue;
+    }
   }
+  int item0 = 0;
+  for (int c = 0; c < kDecClasses; ++c) {
+    const int n = hp.n_dec_class[c];
+    if (n == 0) continue;
+    cudaError_t e = cudaSuccess;
+    switch (c) {
+      case 0: e = launch_mma<T, D, 0>(a, m, kp, use_tma, item0, n); break;
+      case 1: e = launch_mma<T, D, 1>(a, m, kp, use_tma, item0, n); break;
+      case 2: e = launch_mma<T, D, 2>(a, m, kp, use_tma, item0, n); break;
+      default: e = launch_mma<T, D, 3>(a, m, kp, use_tma, item0, n); break;
+    }
+    if (e != cudaSuccess) return e;
+    item0 += n;
+  }
+  return item0 == hp.n_dec ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace

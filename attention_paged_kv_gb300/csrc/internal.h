@@ -19,6 +19,8 @@ struct HostPlan {
   std::vector<int32_t> blob;
   int32_t B = 0, Hq = 0, Hkv = 0, D = 0, ps = 0, num_pages = 0, dtype = 0, causal = 1, T = 0, nnz = 0;
   int32_t n_dec = 0, n_pre = 0, n_merge = 0, n_part = 0, G = 1, num_sms = 0;
+  int32_t dec_cores = 0;                  // 1: decode items run on the CUDA-core kernel
+  int32_t n_dec_class[4] = {0, 0, 0, 0};  // decode items per row class, consecutive in item order
   size_t blob_bytes = 0, off_part_o = 0, off_part_lse = 0, total_bytes = 0;
   size_t off_pages = 0, off_req = 0, off_dec = 0, off_pre = 0, off_merge = 0;
   std::vector<int64_t> kv_len;  // per request (debug gather sizes)
@@ -30,7 +32,7 @@ struct PlanInputs {
   const int32_t* kv_page_indices;
   const int32_t* kv_last_page_len;
   int32_t B, Hq, Hkv, D, ps, num_pages, dtype, causal;
-  int32_t num_sms, force_prefill, decode_chunk_pages, prefill_chunk_tiles;
+  int32_t num_sms, force_prefill, decode_chunk_pages, prefill_chunk_tiles, decode_cuda_cores;
 };
 
 // Validate and partition; on failure returns the status and fills `err`.
@@ -46,7 +48,6 @@ struct RunArgs {
   float* lse;
   cudaStream_t stream;
   int force_cp_async;
-  int decode_cuda_cores;  // 1: G in {4, 8} decodes on the CUDA-core kernel
 };
 
 cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const CUtensorMap* map_q);
@@ -73,7 +74,6 @@ struct pagedattn_plan_s {
   size_t workspace_bytes = 0;
   int device = -1;
   int force_cp_async = 0;
-  int decode_cuda_cores = 0;
   // tensor maps over the last kv_cache pointer seen by run()
   const void* map_kv = nullptr;
   CUtensorMap map_rows;   // decode: box {64, 1, min(ps, 64), 1}, 128-byte swizzle (page_size >= 8)

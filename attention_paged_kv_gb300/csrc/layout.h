@@ -10,13 +10,16 @@ enum HdrIdx : int {
   H_MAGIC = 0, H_VERSION, H_B, H_HQ, H_HKV, H_D, H_PS, H_NUM_PAGES, H_DTYPE, H_CAUSAL,
   H_T, H_NNZ, H_NDEC, H_NPRE, H_NMERGE, H_NPART, H_DEC_CHUNK, H_PRE_CHUNK, H_NUM_SMS, H_G,
   H_OFF_PAGES, H_OFF_REQ, H_OFF_DEC, H_OFF_PRE, H_OFF_MERGE, H_BLOB_BYTES, H_OFF_PART_O,
-  H_OFF_PART_LSE, H_TOTAL_BYTES,
+  H_OFF_PART_LSE, H_TOTAL_BYTES, H_DEC_CORES,
   H_STATUS = 32,
+  H_NDEC_CLASS0 = 33,  // decode items per row class (<= 8, 16, 32, 64 rows), in item order
   HDR_WORDS = 64
 };
 
 constexpr int32_t kMagic = 0x50414731;
-constexpr int32_t kVersion = 1;
+constexpr int32_t kVersion = 2;
+constexpr int kDecClasses = 4;
+constexpr int kDecMaxRows = 64;  // packed (token, head) rows of a small-query item
 constexpr int kQRows = 128;   // packed query rows per prefill MMA tile
 constexpr int kItemRows = 256;  // packed query rows per prefill work item (two tiles)
 constexpr int kKvTile = 128;  // keys per prefill key tile

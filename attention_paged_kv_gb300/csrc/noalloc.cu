@@ -61,8 +61,9 @@ extern "C" pagedattn_status pagedattn_run_decode_noalloc(pagedattn_plan_t plan, 
   const HostPlan& hp = plan->hp;
   if (hp.n_pre > 0)
     return set_err(PA_ERR_UNSUPPORTED,
-                   "pagedattn_run_decode_noalloc runs decode batches only: every request needs qo_len 0 or 1 and "
-                   "num_qo_heads / num_kv_heads in {1, 2, 4, 8}, without force_prefill");
+                   "pagedattn_run_decode_noalloc runs decode batches only: every request needs qo_len 0 or "
+                   "qo_len * G <= 64 with G = num_qo_heads / num_kv_heads in {1, 2, 4, 8, 16}, without "
+                   "force_prefill");
   if (hp.total_bytes > kNoallocScratchBytes)
     return set_err(PA_ERR_WORKSPACE_TOO_SMALL,
                    "this batch needs " + std::to_string(hp.total_bytes) + " bytes of metadata and partial states; "
@@ -97,7 +98,6 @@ extern "C" pagedattn_status pagedattn_run_decode_noalloc(pagedattn_plan_t plan, 
   a.out = out;
   a.lse = lse;
   a.stream = st;
-  a.decode_cuda_cores = plan->decode_cuda_cores;
   e = launch_decode(a, hp.ps >= 8 ? &map : nullptr);
   if (e != cudaSuccess) return cuda_err(e, "no-alloc decode launch");
   e = launch_merge(a);

@@ -8,12 +8,25 @@
 //  1. Per request b: qo_b = qo_indptr[b+1] - qo_indptr[b], pages_b likewise,
 //     kv_b = (pages_b - 1) * page_size + last_b (every page full except the
 //     last, 1 <= last <= page_size as the timing script's comment requires).
-//  2. qo_b == 1 with group size G = Hq/Hkv in {1, 2, 4, 8} -> decode kernel
-//     (CUDA cores); every other request with rows -> tensor-core prefill.
-//  3. Decode split ("kv-parallelism" / split-k in the same issue): chunk =
+//  2. Small-query requests go to the decode kernels: with group size
+//     G = Hq/Hkv in {1, 2, 4, 8, 16}, a request whose R_b = qo_b * G packed
+//     (token, head) rows number at most 64 (one decoded token, or a few
+//     speculative ones), unless force_prefill.  With decode_cuda_cores only
+//     qo_b == 1 at G <= 8 qualifies (the CUDA-core kernel's shapes).  Every
+//     other request with rows -> tensor-core prefill.  The decode items run
+//     on the CUDA-core kernel when decode_cuda_cores is set, or when G <= 2
+//     and every small-query request has qo_b == 1; else on the warp-MMA
+//     kernel.  Row class of an item: R_b <= 8, 16, 32 or 64.
+//  3. Decode split ("kv-parallelism" / split-k in the same issue): chunk c0 =
 //     clamp(ceil(P_dec / (4 * SMs)), 256 keys, 2048 keys) in whole pages,
-//     P_dec = sum of decode pages x Hkv.  Each (request, kv head) is cut at
-//     multiples of the chunk.
+//     P_dec = sum of decode pages x Hkv.  With N(c) = sum over (request,
+//     kv head) of ceil(pages_b / c) items: if N(c0) exceeds one wave of
+//     2 * SMs resident CTAs but some c <= 2048 keys gives N(c) <= 2 * SMs,
+//     the smallest such c is taken (a small batch then runs in one wave).
+//     Each (request, kv head) is cut into n = ceil(pages_b / c) splits of
+//     floor-spaced page boundaries (split s starts at page
+//     floor(s * pages_b / n)), so the splits of a request differ by at most
+//     one page.
 //  4. Prefill: items of 256 packed rows = 256/G tokens x G heads of one kv
 //     head, run as two 128-row MMA tiles that share every K/V tile load (as
 //     do the G heads).  An item needs keys [0, kv_b - qo_b + t0 + n) under
@@ -23,10 +36,13 @@
 //     total key-tile count W exceeds 2 x SMs x chunk: chunk = max(8,
 //     ceil(W / (2 * SMs))) key tiles.
 //  5. Partial fp32 rows are numbered in emission order (decode splits, then
-//     prefill splits); one merge entry per (query token, kv head) of a
+//     prefill splits); a split group of S splits with R rows each takes S*R
+//     consecutive rows; one merge entry per (query token, kv head) of a
 //     split group.
-//  6. Items sorted by decreasing key count, ties in emission order, so the
-//     in-order block dispatch starts the longest items first.
+//  6. Decode items sorted by row class, then by decreasing key count;
+//     prefill items by decreasing key count; ties in emission order.  The
+//     in-order block dispatch starts the longest items first, and each row
+//     class is one launch over consecutive items.
 #include <algorithm>
 #include <cstring>
 #include <string>
@@ -42,7 +58,10 @@ namespace {
 inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 inline int64_t align256(int64_t x) { return cdiv(x, 256) * 256; }
 
-struct DecTmp { int32_t req, kvh, t0, t1, part; };
+struct DecTmp { int32_t req, kvh, t0, t1, part, cls; };
+
+// Row class of a small-query item with R packed rows: 0..3 for <= 8, 16, 32, 64.
+inline int32_t row_class(int64_t R) { return R <= 8 ? 0 : R <= 16 ? 1 : R <= 32 ? 2 : 3; }
 struct PreTmp { int32_t req, kvh, qt0, n, k0, k1, part; };
 
 pagedattn_status fail(std::string* err, pagedattn_status s, const std::string& m) {
@@ -100,9 +119,17 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   }
   const int32_t T = B > 0 ? in.qo_indptr[B] : 0;
 
-  const bool dec_group = (G == 1 || G == 2 || G == 4 || G == 8);
+  const bool dec_group = (G == 1 || G == 2 || G == 4 || G == 8 || G == 16);
   std::vector<char> is_dec(B, 0);
-  for (int b = 0; b < B; ++b) is_dec[b] = (req[b].qo == 1 && dec_group && !in.force_prefill) ? 1 : 0;
+  bool multi_tok = false;
+  for (int b = 0; b < B; ++b) {
+    const int64_t qo = req[b].qo;
+    bool d = qo >= 1 && dec_group && !in.force_prefill && qo * G <= kDecMaxRows;
+    if (in.decode_cuda_cores) d = d && qo == 1 && G <= 8;
+    is_dec[b] = d ? 1 : 0;
+    if (d && qo > 1) multi_tok = true;
+  }
+  const int32_t dec_cores = (in.decode_cuda_cores || (G <= 2 && !multi_tok)) ? 1 : 0;
 
   // -- rule 3: decode items
   int64_t p_dec = 0;
@@ -112,22 +139,43 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   int64_t chunk = in.decode_chunk_pages > 0
                       ? in.decode_chunk_pages
                       : std::min(std::max(cdiv(p_dec, int64_t(4) * in.num_sms), lo), hi);
+  if (in.decode_chunk_pages <= 0 && p_dec > 0) {
+    const int64_t wave = int64_t(2) * in.num_sms;
+    auto items_at = [&](int64_t c) {
+      int64_t n = 0;
+      for (int b = 0; b < B; ++b)
+        if (is_dec[b]) n += cdiv(req[b].np, c) * Hkv;
+      return n;
+    };
+    if (items_at(chunk) > wave && items_at(hi) <= wave) {
+      int64_t a = chunk, z = hi;  // items_at(a) > wave >= items_at(z); items_at is nonincreasing
+      while (z - a > 1) {
+        const int64_t mid = (a + z) / 2;
+        if (items_at(mid) <= wave) z = mid; else a = mid;
+      }
+      chunk = z;
+    }
+  }
   int64_t part = 0;
   std::vector<DecTmp> dec;
   std::vector<MergeEntry> merges;
   for (int b = 0; b < B; ++b) {
     if (!is_dec[b]) continue;
     const int64_t ns = cdiv(req[b].np, chunk);
+    const int64_t R = int64_t(req[b].qo) * G;
+    const int64_t qs = in.qo_indptr[b];
     for (int h = 0; h < Hkv; ++h) {
       const int64_t base = ns > 1 ? part : -1;
       if (ns > 1) {
-        part += ns * G;
-        merges.push_back({int32_t(int64_t(in.qo_indptr[b]) * Hq + h * G), int32_t(base), int32_t(ns), G});
+        part += ns * R;
+        for (int32_t k = 0; k < req[b].qo; ++k)
+          merges.push_back({int32_t((qs + k) * Hq + h * G), int32_t(base + int64_t(k) * G), int32_t(ns),
+                            int32_t(R)});
       }
       for (int64_t s = 0; s < ns; ++s) {
-        const int64_t t0 = s * chunk * ps;
-        const int64_t t1 = std::min<int64_t>((s + 1) * chunk * ps, req[b].kv);
-        dec.push_back({b, h, int32_t(t0), int32_t(t1), ns > 1 ? int32_t(base + s * G) : -1});
+        const int64_t t0 = (s * req[b].np / ns) * ps;
+        const int64_t t1 = std::min<int64_t>(((s + 1) * req[b].np / ns) * ps, req[b].kv);
+        dec.push_back({b, h, int32_t(t0), int32_t(t1), ns > 1 ? int32_t(base + s * R) : -1, row_class(R)});
       }
     }
   }
@@ -173,8 +221,12 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   if (part > INT32_MAX / 256) return fail(err, PA_ERR_UNSUPPORTED, "too many partial rows");
 
   // -- rule 6: longest first, stable
-  std::stable_sort(dec.begin(), dec.end(),
-                   [](const DecTmp& a, const DecTmp& b) { return (a.t1 - a.t0) > (b.t1 - b.t0); });
+  std::stable_sort(dec.begin(), dec.end(), [](const DecTmp& a, const DecTmp& b) {
+    if (a.cls != b.cls) return a.cls < b.cls;
+    return (a.t1 - a.t0) > (b.t1 - b.t0);
+  });
+  int32_t n_class[kDecClasses] = {0, 0, 0, 0};
+  for (const DecTmp& d : dec) ++n_class[d.cls];
   std::stable_sort(pre.begin(), pre.end(),
                    [](const PreTmp& a, const PreTmp& b) { return (a.k1 - a.k0) > (b.k1 - b.k0); });
 
@@ -197,8 +249,9 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
                          int32_t(part), int32_t(chunk), int32_t(ctiles), in.num_sms, G,
                          int32_t(off_pages), int32_t(off_req), int32_t(off_dec), int32_t(off_pre),
                          int32_t(off_merge), int32_t(blob_bytes), int32_t(off_part_o),
-                         int32_t(off_part_lse), int32_t(total)};
+                         int32_t(off_part_lse), int32_t(total), dec_cores};
   std::memcpy(blob.data(), hdr, sizeof(hdr));
+  for (int c = 0; c < kDecClasses; ++c) blob[H_NDEC_CLASS0 + c] = n_class[c];
   if (nnz) std::memcpy(blob.data() + off_pages / 4, in.kv_page_indices, size_t(4 * nnz));
   for (int b = 0; b < B; ++b) {
     int32_t* r = blob.data() + off_req / 4 + 4 * b;
@@ -225,6 +278,8 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   hp->dtype = in.dtype; hp->causal = in.causal ? 1 : 0; hp->T = T; hp->nnz = int32_t(nnz);
   hp->n_dec = int32_t(dec.size()); hp->n_pre = int32_t(pre.size()); hp->n_merge = int32_t(merges.size());
   hp->n_part = int32_t(part); hp->G = G; hp->num_sms = in.num_sms;
+  hp->dec_cores = dec_cores;
+  for (int c = 0; c < kDecClasses; ++c) hp->n_dec_class[c] = n_class[c];
   hp->blob_bytes = size_t(blob_bytes); hp->off_part_o = size_t(off_part_o);
   hp->off_part_lse = size_t(off_part_lse); hp->total_bytes = size_t(total);
   hp->off_pages = size_t(off_pages); hp->off_req = size_t(off_req); hp->off_dec = size_t(off_dec);

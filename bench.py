@@ -43,6 +43,7 @@ WORKLOADS = {
     "decode": lambda wl: wl.decode(),
     "ragged": lambda wl: wl.ragged(),
     "prefix": lambda wl: wl.prefix(),
+    "specdec": lambda wl: wl.mixed(prefill_len=0, decode_qo=4),
 }
 METRIC = "paged-attn prefill TFLOP/s & decode KV GB/s on 1 GB300, % of roofline"
 UNIT = "% of roofline"
@@ -64,13 +65,17 @@ def visible_pairs(qo_lens, kv_lens, causal=True) -> int:
 
 def accounting(w):
     """Algorithmic flops and bytes of the step, split into the prefill part
-    (requests with qo_len > 1) and the decode part (qo_len == 1)."""
+    (requests the planner gives to the tcgen05 prefill kernel) and the decode
+    part (single-token and small-query requests: qo_len * G <= 64 packed rows
+    at a group size G of 1, 2, 4, 8 or 16)."""
     qo = np.diff(w.qo_indptr).astype(np.int64)
     kv = np.asarray(w.gen_kv_lens, np.int64)
     npg = np.diff(w.kv_page_indptr).astype(np.int64)
     D, Hq, Hkv, e = w.head_dim, w.num_qo_heads, w.num_kv_heads, 2
+    G = Hq // Hkv
+    small = (qo >= 1) & (qo * G <= 64) & (G in (1, 2, 4, 8, 16))
     res = {}
-    for part, sel in (("prefill", qo > 1), ("decode", qo == 1)):
+    for part, sel in (("prefill", (qo >= 1) & ~small), ("decode", small)):
         T = int(qo[sel].sum())
         pairs = visible_pairs(qo[sel], kv[sel], w.causal)
         F = 4 * D * Hq * pairs
@@ -80,6 +85,45 @@ def accounting(w):
     res["flops"] = res["prefill"]["flops"] + res["decode"]["flops"]
     res["bytes"] = res["prefill"]["bytes"] + res["decode"]["bytes"]
     return res
+
+
+L2_BYTES = 129 * 10 ** 6  # GB300 L2
+
+
+def rotation_count(w) -> int:
+    """Copies of the step's inputs and outputs to cycle through so that no
+    step finds the previous step's data in L2: 1 when q + out + the cache
+    already exceed 4x L2 (the mixed batch), else enough copies to pass it."""
+    e = 2
+    step_bytes = (2 * int(w.qo_indptr[-1]) * w.num_qo_heads * w.head_dim * e +
+                  int(np.prod(w.kv_cache.shape)) * e)
+    if step_bytes >= 4 * L2_BYTES:
+        return 1
+    return min(64, -(-4 * L2_BYTES // step_bytes))
+
+
+def graph_ms(plan, bufs, stages, reps):
+    """Mean device time of one pass of `stages` per input copy: a CUDA graph
+    holds one pass over every copy in `bufs`; it is replayed `reps` times
+    between two events (no host launch gaps inside the timed region)."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.graph(g, stream=side):
+        h = torch.cuda.current_stream().cuda_stream
+        for q_, kv_, o_, l_ in bufs:
+            plan.run_ptrs(q_.data_ptr(), kv_.data_ptr(), o_.data_ptr(), l_.data_ptr(), h, stages)
+    g.replay()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(reps):
+        g.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / (reps * len(bufs))
 
 
 def load_peaks():
@@ -229,6 +273,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--decode-chunk-pages", type=int, default=0, help="planner override (0: the plan's rule)")
+    ap.add_argument("--prefill-chunk-tiles", type=int, default=0, help="planner override (0: the plan's rule)")
     ap.add_argument("--workload", default="mixed", choices=list(WORKLOADS),
                     help="mixed is the benchmark; the others exist for profiling captures")
     args = ap.parse_args()
@@ -287,53 +333,74 @@ def main():
     lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    need = pa.workspace_size(**w.plan_args(), dtype=w.dtype)
+    popts = {"decode_chunk_pages": args.decode_chunk_pages, "prefill_chunk_tiles": args.prefill_chunk_tiles}
+    need = pa.workspace_size(**w.plan_args(), dtype=w.dtype, **popts)
     ws = torch.empty(max(need, pa.DEFAULT_WORKSPACE_BYTES), dtype=torch.uint8, device=dev)
     t_plan0 = time.perf_counter()
-    plan = pa.Plan(**w.plan_args(), dtype=w.dtype, workspace=ws)
+    plan = pa.Plan(**w.plan_args(), dtype=w.dtype, workspace=ws, **popts)
     t_plan = time.perf_counter() - t_plan0
     hdr = plan.dump()[:32]
     n_dec, n_pre, n_merge = int(hdr[12]), int(hdr[13]), int(hdr[14])
     launches_per_step = int(n_pre > 0) + int(n_dec > 0) + int(n_merge > 0)
+    n_rot = rotation_count(w)
+    bufs = [(q, kv, out, lse)] + [(q.clone(), kv.clone(), torch.empty_like(out), torch.empty_like(lse))
+                                  for _ in range(n_rot - 1)]
     qp, kvp, op, lp = q.data_ptr(), kv.data_ptr(), out.data_ptr(), lse.data_ptr()
 
-    def step():
-        plan.run_ptrs(qp, kvp, op, lp, sh)
-
     for _ in range(args.warmup):
-        step()
+        for q_, kv_, o_, l_ in bufs:
+            plan.run_ptrs(q_.data_ptr(), kv_.data_ptr(), o_.data_ptr(), l_.data_ptr(), sh)
     torch.cuda.synchronize()
     assert plan.device_status() == 0, pa.last_error()
 
-    # per-kernel durations: events between the stages of each step
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
     clk = ClockSampler(dev.index)
-    if world > 1:
-        torch.distributed.barrier()
-    torch.cuda.synchronize()
-    clk.start()
-    t_start = torch.cuda.Event(enable_timing=True)
-    t_end = torch.cuda.Event(enable_timing=True)
-    t_start.record(stream)
-    for i in range(K):
-        e = ev[i]
-        e[0].record(stream)
-        plan.run_ptrs(qp, kvp, op, lp, sh, pa.PA_STAGE_PREFILL)
-        e[1].record(stream)
-        plan.run_ptrs(qp, kvp, op, lp, sh, pa.PA_STAGE_DECODE)
-        e[2].record(stream)
-        plan.run_ptrs(qp, kvp, op, lp, sh, pa.PA_STAGE_MERGE)
-        e[3].record(stream)
-    t_end.record(stream)
-    torch.cuda.synchronize()
-    clocks = clk.stop()
-    if world > 1:
-        torch.distributed.barrier()
-    total_ms = t_start.elapsed_time(t_end)
-    t_pre = sum(e[0].elapsed_time(e[1]) for e in ev) / K
-    t_dec = sum(e[1].elapsed_time(e[2]) for e in ev) / K
-    t_mrg = sum(e[2].elapsed_time(e[3]) for e in ev) / K
+    if n_rot > 1:
+        # small batches: a CUDA graph over n_rot copies of the inputs (so no
+        # step hits the last one's data in L2), replayed between two events;
+        # each stage is then timed the same way on its own
+        reps = max(1, -(-K // n_rot))
+        K = reps * n_rot
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        clk.start()
+        total_ms = graph_ms(plan, bufs, pa.PA_STAGE_ALL, reps) * K
+        clocks = clk.stop()
+        t_pre = graph_ms(plan, bufs, pa.PA_STAGE_PREFILL, reps) if n_pre else 0.0
+        t_dec = graph_ms(plan, bufs, pa.PA_STAGE_DECODE, reps) if n_dec else 0.0
+        t_mrg = graph_ms(plan, bufs, pa.PA_STAGE_MERGE, reps) if n_merge else 0.0
+        if world > 1:
+            torch.distributed.barrier()
+    else:
+        # per-kernel durations: events between the stages of each step
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize()
+        clk.start()
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(K):
+            e = ev[i]
+            e[0].record(stream)
+            plan.run_ptrs(qp, kvp, op, lp, sh, pa.PA_STAGE_PREFILL)
+            e[1].record(stream)
+            plan.run_ptrs(qp, kvp, op, lp, sh, pa.PA_STAGE_DECODE)
+            e[2].record(stream)
+            plan.run_ptrs(qp, kvp, op, lp, sh, pa.PA_STAGE_MERGE)
+            e[3].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        clocks = clk.stop()
+        if world > 1:
+            torch.distributed.barrier()
+        total_ms = t_start.elapsed_time(t_end)
+        # a stage with no items launches nothing: its event pair only measures the gap
+        t_pre = sum(e[0].elapsed_time(e[1]) for e in ev) / K if n_pre else 0.0
+        t_dec = sum(e[1].elapsed_time(e[2]) for e in ev) / K if n_dec else 0.0
+        t_mrg = sum(e[2].elapsed_time(e[3]) for e in ev) / K if n_merge else 0.0
     assert plan.device_status() == 0, pa.last_error()
     if world > 1:
         tt = torch.tensor([total_ms], device=dev)
@@ -373,7 +440,7 @@ def main():
     # end to end through the public API: plan + pinned H2D of q + run + D2H of out/lse
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, max(1, args.e2e_steps), world, dev, hdr)
+        e2e = measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, max(1, args.e2e_steps), world, dev, hdr, popts)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -388,8 +455,10 @@ def main():
                 "dtype": "bf16", "data": "synthetic",
                 "config": {"workload": WORKLOAD_DESC.get(args.workload, args.workload),
                            "parallelism": "replica per GPU" if world > 1 else "1 GPU",
-                           "l2": "no flush: the 4.6 GB KV cache is 35x the 129 MB L2 and the decode pass "
-                                 "streams it between consecutive prefills",
+                           "l2": ("no flush: the 4.6 GB KV cache is 35x the 129 MB L2 and the decode pass "
+                                  "streams it between consecutive prefills") if n_rot == 1 else
+                                 (f"inputs larger than L2: {n_rot} copies of q, out and the cache, cycled by "
+                                  f"a CUDA graph of one step per copy"),
                            "roofline_time_ms": roof_t * 1e3, "plan_ms": t_plan * 1e3,
                            "items": {"prefill": n_pre, "decode": n_dec, "merge": n_merge}},
                 "roofline": roof, "prefill": prefill_obj, "decode": decode_obj,
@@ -402,10 +471,18 @@ def main():
 WORKLOAD_DESC = {
     "mixed": "mixed serving step: 1 causal prefill of 8192 tokens + 256 decodes with kv_len U[512,8192]; "
              "Hq 64 / Hkv 8, head_dim 128, page_size 16, bf16, random physical pages",
+    "decode": "decode timing script: 128 requests x 1 query token, 1024 keys each; Hq 8 / Hkv 1, head_dim 128, "
+              "page_size 16, fp16, contiguous pages",
+    "ragged": "ragged prefill: 32 prompts of U[16,200] tokens, qo = kv; Hq 32 / Hkv 8, head_dim 128, "
+              "page_size 16, bf16",
+    "prefix": "prefix sharing: 64 requests appending 30 tokens to one 200-token prompt (12 shared pages); "
+              "Hq 32 / Hkv 8, head_dim 128, page_size 16, bf16",
+    "specdec": "speculative decoding: 256 requests x 4 query tokens, kv_len U[512,8192]; Hq 64 / Hkv 8, "
+               "head_dim 128, page_size 16, bf16",
 }
 
 
-def measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, E, world, dev, hdr):
+def measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, E, world, dev, hdr, popts):
     import torch
     q_h = w.q.pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
@@ -413,7 +490,7 @@ def measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, E, world, dev, hdr):
     args_plan = w.plan_args()
 
     def e2e_step():
-        p2 = pa.Plan(**args_plan, dtype=w.dtype, workspace=ws)
+        p2 = pa.Plan(**args_plan, dtype=w.dtype, workspace=ws, **popts)
         q.copy_(q_h, non_blocking=True)
         p2.run(q, kv, out=out, lse=lse)
         out_h.copy_(out, non_blocking=True)

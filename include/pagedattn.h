@@ -77,12 +77,14 @@ typedef enum { PA_FP16 = 0, PA_BF16 = 1 } pagedattn_dtype;
 /* Optional planner settings; pass NULL for the defaults (all zero). */
 typedef struct {
   int32_t num_sms;             /* SMs to plan for; 0 = ask the current device        */
-  int32_t force_prefill;       /* 1: qo_len == 1 requests use the tensor-core kernel */
+  int32_t force_prefill;       /* 1: every request uses the tcgen05 prefill kernel    */
   int32_t decode_chunk_pages;  /* > 0: pages per decode split (default: see plan)    */
   int32_t prefill_chunk_tiles; /* > 0: 128-key tiles per prefill split               */
   int32_t force_cp_async;      /* 1: stage prefill K/V with cp.async instead of TMA   */
-  int32_t decode_cuda_cores;   /* 1: decode groups of 4 or 8 query heads per kv head
-                                  on the CUDA-core kernel (default: warp-level MMA)  */
+  int32_t decode_cuda_cores;   /* 1: single-token requests at group sizes <= 8 run on
+                                  the CUDA-core decode kernel, and multi-token
+                                  requests all go to the prefill kernel (default:
+                                  the warp-MMA small-query kernel, see plan)        */
   int32_t reserved[2];         /* must be 0                                          */
 } pagedattn_options;
 
@@ -155,9 +157,10 @@ PAGEDATTN_API pagedattn_status pagedattn_workspace_size(const int32_t* qo_indptr
  * lse      device, float[T, Hq] natural-log sums, or NULL to skip.
  * stream   the stream every kernel is queued on.
  *
- * Launches the prefill kernel (tcgen05 / TMEM), the decode kernel (CUDA
- * cores) and, when some request was split, the merge kernel, in that order on
- * `stream`.  Allocates nothing and does not synchronise the host.  In-kernel
+ * Launches the prefill kernel (tcgen05 / TMEM), the small-query kernels
+ * (decode and requests of qo_len * G <= 64 rows: warp-level MMA, one launch
+ * per row class, or the CUDA-core decode kernel) and, when some request was
+ * split, the merge kernel, in that order on `stream`.  Allocates nothing and does not synchronise the host.  In-kernel
  * waits are bounded; a wait that gives up sets PA_DEV_TIMEOUT in the device
  * status word (read it with pagedattn_device_status).  Calls that overlap on
  * the device must use different workspaces (the partial states live there).
@@ -221,9 +224,10 @@ PAGEDATTN_API pagedattn_status pagedattn_debug_gather(pagedattn_plan_t plan, int
  * library and stays allocated until the process exits.  q, kv_cache, out and
  * lse are as for pagedattn_run.
  *
- * The batch must be decode-only (every request has qo_len 0 or 1, the group
- * size num_qo_heads / num_kv_heads is 1, 2, 4 or 8, and force_prefill is
- * off): PA_ERR_UNSUPPORTED otherwise.  A plan whose metadata and partial
+ * The batch must have no prefill items (every request has qo_len 0 or
+ * qo_len * G <= 64 with the group size G = num_qo_heads / num_kv_heads in
+ * {1, 2, 4, 8, 16}, and force_prefill is off; with decode_cuda_cores,
+ * qo_len <= 1 and G <= 8): PA_ERR_UNSUPPORTED otherwise.  A plan whose metadata and partial
  * states exceed 16 MiB returns PA_ERR_WORKSPACE_TOO_SMALL (plan with a larger
  * decode_chunk_pages).  The call allocates no memory.  Its first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) while

@@ -12,15 +12,26 @@ Rules (the planner is deterministic; nothing depends on timing):
 
 1. Per request: qo_b, pages_b, kv_b = (pages_b - 1) * page_size + last_b
    (see ``oracle.attention.kv_len_of``), page_start_b.
-2. A request with qo_b == 1 goes to the decode kernel when G = Hq/Hkv is one
-   of 1, 2, 4, 8 (and ``force_prefill`` is off); every other request with
-   qo_b >= 1 goes to the tensor-core prefill kernel.
+2. Small-query requests go to the decode kernels: G = Hq/Hkv is one of
+   1, 2, 4, 8, 16, the request's R_b = qo_b * G packed (token, head) rows
+   number at most 64, and ``force_prefill`` is off.  With
+   ``decode_cuda_cores`` only qo_b == 1 at G <= 8 qualifies.  Every other
+   request with qo_b >= 1 goes to the tensor-core prefill kernel.  The
+   decode items run on CUDA cores (header word 29 = 1) when
+   ``decode_cuda_cores`` is set, or when G <= 2 and no small-query request
+   has qo_b > 1; else on the warp-MMA kernel (0).  An item's row class is
+   0, 1, 2, 3 for R_b <= 8, 16, 32, 64.
 3. Decode split ("kv-parallelism", the split-k of the same issue): with
    P_dec = sum over decode requests of pages_b * Hkv and
-   target = 4 * num_sms, the chunk is
-   clamp(ceil(P_dec / target), max(1, 256 // page_size), max(1, 2048 // page_size))
-   pages (or the override).  Request b is cut into ceil(pages_b / chunk)
-   splits at page boundaries, for every kv head.
+   target = 4 * num_sms, the first choice is
+   c0 = clamp(ceil(P_dec / target), lo = max(1, 256 // page_size),
+   hi = max(1, 2048 // page_size)) pages.  Let N(c) = sum over decode
+   requests of Hkv * ceil(pages_b / c), the item count at chunk c.  If
+   N(c0) > 2 * num_sms (more than one wave of resident CTAs) and
+   N(hi) <= 2 * num_sms, the chunk is the smallest c with N(c) <= 2 * num_sms;
+   else c0 (an override replaces both).  Request b is cut into
+   n = ceil(pages_b / chunk) splits, split s covering pages
+   [floor(s * pages_b / n), floor((s + 1) * pages_b / n)), for every kv head.
 4. Prefill items: 256 packed rows = (256 / G) query tokens x G heads (two
    128-row tiles).  Item [t0, t0 + n) of request b needs keys [0, e) with
    e = kv_b - qo_b + t0 + n (causal) or kv_b; that is ceil(e / 128) key
@@ -31,21 +42,25 @@ Rules (the planner is deterministic; nothing depends on timing):
 5. Partial rows (fp32, in the workspace) are handed out in emission order:
    decode splits first (request, then kv head), then prefill splits (request,
    tile, kv head); a split group of S splits and R rows per split takes S * R
-   consecutive rows.  One merge entry is emitted per (query token, kv head)
-   of a split group: {out_row0, part_row0, nsplit, split_stride}.
-6. Items are then ordered by decreasing key count (longest first), ties in
-   emission order (a stable sort), so that the hardware's in-order block
-   dispatch spreads the long items first.
+   consecutive rows (R = R_b for decode items).  One merge entry is emitted
+   per (query token, kv head) of a split group: {out_row0, part_row0,
+   nsplit, split_stride}.
+6. Decode items are then ordered by row class, then by decreasing key count;
+   prefill items by decreasing key count; ties keep emission order (stable
+   sorts).  The hardware's in-order block dispatch so starts the long items
+   first, and each row class is one launch over consecutive items; header
+   words 33..36 hold the number of decode items of each class.
 
 Metadata layout (int32 words, every region 256-byte aligned), which is what
 ``pagedattn_debug_plan_dump`` returns and ``pagedattn_plan`` copies to the
 start of the workspace:
 
-    header[64]  magic 0x50414731, version 1, B, Hq, Hkv, D, page_size,
+    header[64]  magic 0x50414731, version 2, B, Hq, Hkv, D, page_size,
                 num_pages, dtype, causal, T, nnz, n_dec, n_pre, n_merge,
                 n_part_rows, dec_chunk_pages, pre_chunk_tiles, num_sms, G,
                 off_pages, off_req, off_dec, off_pre, off_merge, blob_bytes,
-                off_part_o, off_part_lse, total_bytes, 0..., [32] status word
+                off_part_o, off_part_lse, total_bytes, dec_cuda_cores, 0, 0,
+                [32] status word, [33..36] decode items per row class, 0...
     pages[nnz]       copy of kv_page_indices
     req[B][4]        qo_start, qo_len, kv_len, page_start
     dec[n_dec][8]    req, kv_head, tok0, tok1, part_row(-1 = direct), 0, 0, 0
@@ -59,16 +74,19 @@ import numpy as np
 from .attention import PlanError, request_lengths
 
 MAGIC = 0x50414731
-VERSION = 1
+VERSION = 2
 HDR_WORDS = 64
 STATUS_WORD = 32
 Q_ROWS = 128       # packed query rows per prefill MMA tile (G must divide it)
 ITEM_ROWS = 256    # packed query rows per prefill work item
 KV_TILE = 128      # keys per prefill key tile
 DEC_ITEMS_PER_SM = 4
+DEC_WAVE_PER_SM = 2   # resident small-query CTAs per SM
 PRE_ITEMS_PER_SM = 2
 PRE_MIN_CHUNK_TILES = 8
-DECODE_GROUPS = (1, 2, 4, 8)
+DECODE_GROUPS = (1, 2, 4, 8, 16)
+DEC_MAX_ROWS = 64
+DEC_CLASS_ROWS = (8, 16, 32, 64)
 
 FP16, BF16 = 0, 1
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED = 0, 1, 2
@@ -88,7 +106,7 @@ def _align(x, a=256):
 
 def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_heads,
           num_kv_heads, head_dim, page_size, num_pages, dtype=BF16, causal=True, num_sms=148,
-          force_prefill=False, decode_chunk_pages=0, prefill_chunk_tiles=0):
+          force_prefill=False, decode_chunk_pages=0, prefill_chunk_tiles=0, decode_cuda_cores=False):
     """Return the metadata blob (np.int32) the planner must produce."""
     Hq, Hkv, D, ps = int(num_qo_heads), int(num_kv_heads), int(head_dim), int(page_size)
     if Hq < 1 or Hkv < 1 or Hq % Hkv:
@@ -118,28 +136,46 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
             raise PlanError("query rows without keys")
     T = int(np.asarray(qo_indptr)[-1])
 
-    is_dec = [qo == 1 and G in DECODE_GROUPS and not force_prefill for (qo, _, _, _) in lens]
+    is_dec = []
+    for (qo, _, _, _) in lens:
+        d = qo >= 1 and G in DECODE_GROUPS and not force_prefill and qo * G <= DEC_MAX_ROWS
+        if decode_cuda_cores:
+            d = d and qo == 1 and G <= 8
+        is_dec.append(d)
+    multi = any(d and l[0] > 1 for l, d in zip(lens, is_dec))
+    dec_cores = 1 if (decode_cuda_cores or (G <= 2 and not multi)) else 0
 
     # -- decode items (rule 3)
     p_dec = sum(l[3] * Hkv for l, d in zip(lens, is_dec) if d)
     lo, hi = max(1, 256 // ps), max(1, 2048 // ps)
     chunk = decode_chunk_pages if decode_chunk_pages > 0 else min(max(_cdiv(p_dec, DEC_ITEMS_PER_SM * num_sms), lo), hi)
+    if decode_chunk_pages <= 0 and p_dec > 0:
+        wave = DEC_WAVE_PER_SM * num_sms
+
+        def n_items(c):
+            return sum(Hkv * _cdiv(l[3], c) for l, d in zip(lens, is_dec) if d)
+
+        if n_items(chunk) > wave and n_items(hi) <= wave:
+            chunk = next(c for c in range(chunk, hi + 1) if n_items(c) <= wave)
     part = 0
     dec, merges = [], []
     for b, ((qo, kv, p0, npg), d) in enumerate(zip(lens, is_dec)):
         if not d:
             continue
         ns = _cdiv(npg, chunk)
+        R = qo * G
+        cls = next(c for c, rows in enumerate(DEC_CLASS_ROWS) if R <= rows)
+        qs = int(qo_indptr[b])
         for h in range(Hkv):
             base = part if ns > 1 else -1
             if ns > 1:
-                part += ns * G
-                qs = int(qo_indptr[b])
-                merges.append((qs * Hq + h * G, base, ns, G))
+                part += ns * R
+                for t in range(qo):
+                    merges.append(((qs + t) * Hq + h * G, base + t * G, ns, R))
             for s in range(ns):
-                t0 = s * chunk * ps
-                t1 = min((s + 1) * chunk * ps, kv)
-                dec.append((b, h, t0, t1, base + s * G if ns > 1 else -1))
+                t0 = (s * npg // ns) * ps
+                t1 = min(((s + 1) * npg // ns) * ps, kv)
+                dec.append((b, h, t0, t1, base + s * R if ns > 1 else -1, cls))
 
     # -- prefill items (rule 4)
     tq = ITEM_ROWS // G
@@ -170,7 +206,8 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
                 pre.append((b, h, t0, n, k0, k1, base + s * n * G if ns > 1 else -1))
 
     # -- longest first, stable (rule 6)
-    dec = sorted(dec, key=lambda it: -(it[3] - it[2]))
+    dec = sorted(dec, key=lambda it: (it[5], -(it[3] - it[2])))
+    n_class = [sum(1 for it in dec if it[5] == c) for c in range(len(DEC_CLASS_ROWS))]
     pre = sorted(pre, key=lambda it: -(it[5] - it[4]))
 
     # -- layout
@@ -190,14 +227,15 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
     hdr = [MAGIC, VERSION, B, Hq, Hkv, D, ps, num_pages, dtype, int(bool(causal)), T, nnz,
            len(dec), len(pre), len(merges), part, chunk, ctiles, num_sms, G,
            off_pages, off_req, off_dec, off_pre, off_merge, blob_bytes, off_part_o,
-           off_part_lse, total]
+           off_part_lse, total, dec_cores]
     blob[:len(hdr)] = hdr
+    blob[33:33 + len(n_class)] = n_class
     blob[off_pages // 4: off_pages // 4 + nnz] = indices
     req = np.array([(int(qo_indptr[b]), qo, kv, p0) for b, (qo, kv, p0, _) in enumerate(lens)],
                    np.int32).reshape(-1, 4)
     blob[off_req // 4: off_req // 4 + 4 * B] = req.reshape(-1)
     for j, it in enumerate(dec):
-        blob[off_dec // 4 + 8 * j: off_dec // 4 + 8 * j + 5] = it
+        blob[off_dec // 4 + 8 * j: off_dec // 4 + 8 * j + 5] = it[:5]
     for j, it in enumerate(pre):
         blob[off_pre // 4 + 8 * j: off_pre // 4 + 8 * j + 7] = it
     for j, it in enumerate(merges):
@@ -209,8 +247,10 @@ def decode_header(blob: np.ndarray) -> dict:
     names = ["magic", "version", "B", "Hq", "Hkv", "D", "page_size", "num_pages", "dtype",
              "causal", "T", "nnz", "n_dec", "n_pre", "n_merge", "n_part_rows", "dec_chunk_pages",
              "pre_chunk_tiles", "num_sms", "G", "off_pages", "off_req", "off_dec", "off_pre",
-             "off_merge", "blob_bytes", "off_part_o", "off_part_lse", "total_bytes"]
-    return {n: int(blob[i]) for i, n in enumerate(names)}
+             "off_merge", "blob_bytes", "off_part_o", "off_part_lse", "total_bytes", "dec_cuda_cores"]
+    h = {n: int(blob[i]) for i, n in enumerate(names)}
+    h["dec_class_items"] = [int(x) for x in blob[33:33 + len(DEC_CLASS_ROWS)]]
+    return h
 
 
 def items(blob: np.ndarray):

@@ -328,11 +328,18 @@ def test_planted_mistakes(name, monkeypatch):
 @pytest.mark.parametrize("wname,sms,kw", [
     ("tiny", 148, {}), ("tiny", 2, {"prefill_chunk_tiles": 1}), ("decode", 148, {}),
     ("ragged", 148, {}), ("prefix", 148, {}), ("tiny", 148, {"force_prefill": True}),
-    ("custom_long", 4, {}),
+    ("custom_long", 4, {}), ("smallq", 4, {}), ("smallq", 148, {"decode_cuda_cores": True}),
+    ("smallq_g16", 148, {}), ("smallq_g1", 3, {}),
 ])
 def test_plan_ref_covers_every_pair_once(wname, sms, kw):
     if wname == "custom_long":
         w = small([1, 40, 1, 300], [2000, 700, 33, 300], 8, 2, D=64, ps=16, seed=3)
+    elif wname == "smallq":  # G 8: rows 32, 32, 16, 8, 64, and a prefill of 9 tokens
+        w = small([4, 4, 2, 1, 8, 9], [300, 40, 900, 70, 500, 9], 16, 2, D=64, ps=16, seed=4)
+    elif wname == "smallq_g16":  # G 16: rows 16, 32, 64, then prefill
+        w = small([1, 2, 4, 5], [77, 500, 260, 30], 16, 1, D=64, ps=8, seed=5)
+    elif wname == "smallq_g1":  # G 1: up to 64 tokens per small-query item
+        w = small([64, 65, 3, 1], [64, 200, 1000, 9], 2, 2, D=64, ps=4, seed=6)
     elif wname == "decode":
         w = workloads.decode(batch_size=16)
     elif wname == "ragged":
@@ -351,12 +358,16 @@ def test_plan_ref_covers_every_pair_once(wname, sms, kw):
     cover = {}
     lens = A.request_lengths(w.qo_indptr, w.kv_page_indptr, w.kv_last_page_len, w.page_size)
     for (b, hk, t0, t1, pr, *_r) in dec:
-        row = int(w.qo_indptr[b])
-        for g in range(G):
-            for t in range(t0, t1):
-                key = (row, hk * G + g, t)
-                assert key not in cover
-                cover[key] = 1
+        qo, kv = lens[b][0], lens[b][1]
+        assert qo * G <= 64
+        for i in range(qo):
+            vis = kv - qo + i + 1 if w.causal else kv
+            row = int(w.qo_indptr[b]) + i
+            for g in range(G):
+                for t in range(t0, min(t1, vis)):
+                    key = (row, hk * G + g, t)
+                    assert key not in cover
+                    cover[key] = 1
     for (b, hk, qt0, n, k0, k1, pr, _) in pre:
         qo, kv = lens[b][0], lens[b][1]
         for i in range(qt0, qt0 + n):
@@ -381,8 +392,14 @@ def test_plan_ref_covers_every_pair_once(wname, sms, kw):
                 assert 0 <= r < h["n_part_rows"] and r not in rows
                 rows.add(r)
     assert len(rows) == h["n_part_rows"]
-    # longest first
-    assert all(np.diff(dec[:, 3] - dec[:, 2]) <= 0) if len(dec) else True
+    # decode items: grouped by row class (counts in the header), longest first within a class
+    cls = np.array([next(c for c, n in enumerate((8, 16, 32, 64)) if lens[b][0] * G <= n) for b in dec[:, 0]],
+                   np.int64)
+    assert all(np.diff(cls) >= 0)
+    assert h["dec_class_items"] == [int((cls == c).sum()) for c in range(4)]
+    for c in range(4):
+        ln = (dec[:, 3] - dec[:, 2])[cls == c]
+        assert all(np.diff(ln) <= 0)
     assert all(np.diff(pre[:, 5] - pre[:, 4]) <= 0) if len(pre) else True
 
 
@@ -391,6 +408,9 @@ def test_plan_ref_decode_script_split():
     blob = plan_ref.build(**{k: v for k, v in w.plan_args().items() if k != "causal"},
                           dtype=plan_ref.FP16, num_sms=148)
     h = plan_ref.decode_header(blob)
-    # 8192 pages / (4 * 148) -> 14, clamped up to 256 keys = 16 pages: 4 splits
-    assert h["dec_chunk_pages"] == 16 and h["n_dec"] == 512 and h["n_merge"] == 128
-    assert h["n_part_rows"] == 128 * 4 * 8 and h["n_pre"] == 0
+    # 8192 pages / (4 * 148) -> 14, clamped up to 256 keys = 16 pages: 512 items, more than one
+    # wave of 2 * 148; the smallest chunk that fits one wave is 32 pages: 2 splits of 32 pages
+    assert h["dec_chunk_pages"] == 32 and h["n_dec"] == 256 and h["n_merge"] == 128
+    assert h["n_part_rows"] == 128 * 2 * 8 and h["n_pre"] == 0
+    dec, _, _ = plan_ref.items(blob)
+    assert sorted({(int(a), int(b)) for a, b in dec[:, 2:4]}) == [(0, 512), (512, 1024)]

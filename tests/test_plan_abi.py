@@ -56,6 +56,8 @@ CASES = [
     ("decode", {}), ("decode", {"decode_chunk_pages": 3}), ("ragged", {}), ("ragged_padded", {}),
     ("prefix", {}), ("prefix_dup", {}), ("mixed_small", {}), ("mixed_small", {"prefill_chunk_tiles": 2}),
     ("random", {}), ("random_nc", {}), ("empty", {}), ("qo0", {}),
+    ("random", {"decode_cuda_cores": True}), ("smallq", {}), ("smallq", {"decode_cuda_cores": True}),
+    ("smallq", {"decode_chunk_pages": 2}), ("smallq_g16", {}), ("smallq_g1", {}), ("specdec", {}),
 ]
 
 
@@ -79,6 +81,15 @@ def make(name):
                                      dtype=torch.bfloat16, seed=5)
     if name == "random_nc":
         return workloads.make_custom("r", [3, 1, 200], [2, 7, 40], 8, 8, 64, 2, causal=False, seed=6)
+    if name == "smallq":  # G 8: 32, 32, 16, 8 and 64 packed rows, and a 9-token prefill
+        return workloads.make_custom("sq", [4, 4, 2, 1, 8, 9], [300, 40, 900, 70, 500, 9], 16, 2, 128, 16,
+                                     dtype=torch.bfloat16, seed=11)
+    if name == "smallq_g16":
+        return workloads.make_custom("sq16", [1, 2, 4, 5], [77, 500, 260, 30], 16, 1, 64, 8, seed=12)
+    if name == "smallq_g1":
+        return workloads.make_custom("sq1", [64, 65, 3, 1], [64, 200, 1000, 9], 2, 2, 64, 4, seed=13)
+    if name == "specdec":
+        return workloads.mixed(num_decode=24, prefill_len=0, kv_lo=16, kv_hi=3000, decode_qo=4)
     if name == "empty":
         return workloads.make_custom("e", [], [], 4, 1, 64, 16, seed=7)
     if name == "qo0":
@@ -184,14 +195,39 @@ def test_host_only_plan_cannot_run(lib):
 
 
 def test_plan_metadata_semantics(lib):
-    """The decode script's batch splits into 4 x 256-key chunks per request
-    on 148 SMs; the mixed batch keeps its long prefill unsplit."""
+    """The decode script's batch splits into 2 x 512-key chunks per request
+    on 148 SMs (one wave of 256 items); the mixed batch keeps its long
+    prefill unsplit."""
     w = workloads.decode()
     h = plan_ref.decode_header(_lib_blob(w, num_sms=148))
-    assert (h["n_dec"], h["n_pre"], h["n_merge"], h["dec_chunk_pages"]) == (512, 0, 128, 16)
+    assert (h["n_dec"], h["n_pre"], h["n_merge"], h["dec_chunk_pages"]) == (256, 0, 128, 32)
     w = workloads.mixed(num_decode=8, prefill_len=8192, kv_lo=512, kv_hi=8192)
     blob = _lib_blob(w, num_sms=148)
     dec, pre, mer = plan_ref.items(blob)
     assert (pre[:, 6] == -1).all()                 # no prefill split
     assert pre[:, 3].max() == 32                   # 32 tokens x 8 heads per item (two tiles)
     assert pre[0, 5] - pre[0, 4] == 8192           # longest first
+
+
+def test_plan_small_query_semantics(lib):
+    """Requests of a few query tokens (qo_len * G <= 64 packed rows) become
+    small-query items of the decode kernels, grouped by row class; their
+    split groups merge per (token, kv head) with a stride of qo_len * G."""
+    w = workloads.mixed(num_decode=24, prefill_len=0, kv_lo=16, kv_hi=3000, decode_qo=4)
+    blob = _lib_blob(w, num_sms=148, decode_chunk_pages=16)
+    h = plan_ref.decode_header(blob)
+    dec, pre, mer = plan_ref.items(blob)
+    assert h["n_pre"] == 0 and h["dec_cuda_cores"] == 0
+    assert h["dec_class_items"] == [0, 0, h["n_dec"], 0]   # 4 tokens x 8 heads = 32 rows
+    split = dec[dec[:, 4] >= 0]
+    assert len(split) and (mer[:, 3] == 32).all()
+    assert len(mer) == 4 * len({(int(b), int(k)) for b, k in split[:, :2]})
+    # the option keeps multi-token requests on the prefill kernel
+    h2 = plan_ref.decode_header(_lib_blob(w, num_sms=148, decode_cuda_cores=True))
+    assert h2["n_dec"] == 0 and h2["dec_cuda_cores"] == 1
+    # G <= 2 with single-token requests only: CUDA cores; one two-token request moves all to MMA
+    a = workloads.make_custom("g2", [1, 1, 1], [10, 20, 30], 4, 2, 64, 4, seed=1)
+    assert plan_ref.decode_header(_lib_blob(a, num_sms=148))["dec_cuda_cores"] == 1
+    b = workloads.make_custom("g2", [1, 2, 1], [10, 20, 30], 4, 2, 64, 4, seed=1)
+    hb = plan_ref.decode_header(_lib_blob(b, num_sms=148))
+    assert hb["dec_cuda_cores"] == 0 and hb["n_pre"] == 0 and hb["dec_class_items"][0] == hb["n_dec"]

@@ -63,7 +63,8 @@ def test_noalloc_decode_matches_run_two_calls_in_a_row():
 
 def test_noalloc_rejects_prefill_batches():
     lib = pa.load()
-    w = workloads.tiny()
+    w = workloads.make_custom("pre", [1, 40], [9, 300], 16, 2, 128, 16, seed=3)  # 40 x 8 rows: prefill
     plan = pa.Plan(**w.plan_args(), dtype=w.dtype, host_only=True, num_sms=148)
+    assert plan.dump()[13] > 0
     st = lib.pagedattn_run_decode_noalloc(plan._h, None, None, None, None, None)
     assert st == pa.PA_ERR_UNSUPPORTED and "decode" in pa.last_error()

@@ -289,15 +289,18 @@ def prefix(duplicated: bool = False, batch_size: int = 64) -> Workload:
 
 
 def mixed(num_decode: int = 256, prefill_len: int = 8192, kv_lo: int = 512, kv_hi: int = 8192,
-          num_qo_heads: int = 64, num_kv_heads: int = 8) -> Workload:
-    """One causal prefill of ``prefill_len`` tokens (request 0) next to
-    ``num_decode`` one-token decodes with kv_len uniform on [kv_lo, kv_hi];
-    Hq 64 / Hkv 8, head_dim 128, page_size 16, bf16, random page ids."""
+          num_qo_heads: int = 64, num_kv_heads: int = 8, decode_qo: int = 1) -> Workload:
+    """One causal prefill of ``prefill_len`` tokens (request 0; none when 0)
+    next to ``num_decode`` decodes of ``decode_qo`` query tokens each
+    (speculative-decoding shapes when > 1) with kv_len uniform on
+    [kv_lo, kv_hi]; Hq 64 / Hkv 8, head_dim 128, page_size 16, bf16, random
+    page ids."""
     s = _SEEDS["mixed"]
     ps, D = 16, 128
     kvd = randint_incl(kv_lo, kv_hi, num_decode, s * 100 + 1)
-    qo = [prefill_len] + [1] * num_decode
-    kv = [prefill_len] + [int(x) for x in kvd]
+    pre = [prefill_len] if prefill_len > 0 else []
+    qo = pre + [int(decode_qo)] * num_decode
+    kv = pre + [int(x) for x in kvd]
     n = sum(pages_for(k, ps) for k in kv)
     perm = randperm(n, s * 100 + 4)
     tabs = build_tables(qo, kv, ps, perm)
