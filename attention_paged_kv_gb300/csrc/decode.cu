@@ -427,32 +427,17 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode
 //              fragment (a quad of lanes holds a row), whose exp2 values
 //              become the A fragment of P V directly; ldmatrix.trans feeds V.
 //              O stays in registers; the key subsets are combined at the end.
-// Row classes (template RC): 8 rows (RGN 1; the accumulators of the unused
-// rows 8..15 are fed zeros and dropped), 16 rows (RGN 1), 32 (RGN 2) and 64
-// (RGN 4).  Each row's keys end at its own causal limit.  For requests with
+// Row classes (template RC): up to 8 and up to 16 rows (RGN 1; fragment rows
+// past R see no keys), 32 (RGN 2) and 64 (RGN 4); the first two run the same
+// code and differ only in how the planner groups items.  Each row's keys end at its own causal limit.  For requests with
 // fewer than 128 keys P is split into hi + lo halves (two MMAs), as in the
 // prefill kernel, so rows that see few keys keep P's rounding out of the
 // output.
 
 template <typename T>
 struct Mma {
-  // rows 0..7 only: the A registers of rows 8..15 are zero and their
-  // accumulators are fed zeros and dropped (two registers per n-tile)
-  __device__ static __forceinline__ void half(float (&d)[2], const uint32_t (&a)[2], uint32_t b0, uint32_t b1) {
-    float x2, x3;
-    if constexpr (Elt<T>::kBf16)
-      asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-          "{%0, %1, %10, %10};"
-          : "+f"(d[0]), "+f"(d[1]), "=f"(x2), "=f"(x3)
-          : "r"(a[0]), "r"(0u), "r"(a[1]), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
-    else
-      asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
-          "{%0, %1, %10, %10};"
-          : "+f"(d[0]), "+f"(d[1]), "=f"(x2), "=f"(x3)
-          : "r"(a[0]), "r"(0u), "r"(a[1]), "r"(0u), "r"(b0), "r"(b1), "f"(0.f));
-  }
   // all 16 rows; a = {row g cols 2t.., row g cols 2t+8.., row g+8 cols 2t.., row g+8 cols 2t+8..}
-  __device__ static __forceinline__ void full(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
+  __device__ static __forceinline__ void run(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     if constexpr (Elt<T>::kBf16)
       asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
           "{%0, %1, %2, %3};"
@@ -465,14 +450,6 @@ struct Mma {
           : "r"(a[0]), "r"(a[2]), "r"(a[1]), "r"(a[3]), "r"(b0), "r"(b1));
   }
 };
-template <typename T, int NA>
-__device__ __forceinline__ void mma_rows(float (&d)[NA], const uint32_t (&a)[NA], uint32_t b0, uint32_t b1) {
-  if constexpr (NA == 2)
-    Mma<T>::half(d, a, b0, b1);
-  else
-    Mma<T>::full(d, a, b0, b1);
-}
-
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2, uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
@@ -490,12 +467,10 @@ constexpr int kDmThreads = 160;  // 4 MMA warps + 1 producer
 
 template <int RC>
 struct RowClass {
-  static constexpr bool HALF = RC == 0;                        // rows 8..15 unused
   static constexpr int RGN = RC <= 1 ? 1 : (RC == 2 ? 2 : 4);  // row groups of 16
   static constexpr int KS = 4 / RGN;                           // key subsets (warps per row group)
   static constexpr int KW = kDecTile / KS;                     // keys per warp per stage
   static constexpr int NKB = KW / 16;                          // 16-key blocks per warp
-  static constexpr int NA = HALF ? 2 : 4;                      // accumulator registers per n-tile
 };
 
 template <typename T, int D, int RC>
@@ -504,7 +479,8 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
                       const int item0) {
   using C = DecCfg<D>;
   using RCl = RowClass<RC>;
-  constexpr int RGN = RCl::RGN, KS = RCl::KS, KW = RCl::KW, NKB = RCl::NKB, NA = RCl::NA;
+  constexpr int RGN = RCl::RGN, KS = RCl::KS, KW = RCl::KW, NKB = RCl::NKB;
+  constexpr int NA = 4;        // fragment registers per lane: rows lo (0, 1) and hi (2, 3)
   constexpr int NKS = D / 16;  // k-steps of S
   constexpr int NNT = D / 8;   // n-tiles of O
   extern __shared__ uint8_t smem_raw[];
@@ -550,7 +526,7 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
     const int lim = p.causal ? rq.kv_len - rq.qo_len + (r >> p.g_shift) + 1 : rq.kv_len;
     return min(it.tok1, lim);
   };
-  const int end_lo = end_of(r_lo), end_hi = RCl::HALF ? 0 : end_of(r_hi);
+  const int end_lo = end_of(r_lo), end_hi = end_of(r_hi);
 
   // q as A fragments: {row lo cols 2t, row lo cols 2t+8, row hi cols 2t, row hi cols 2t+8} per k-step
   uint32_t qa[NKS][NA];
@@ -566,16 +542,14 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
         qa[kk][1] = __ldg(qp + kk * 8 + 4 + t);
       }
     }
-    if constexpr (NA == 4) {
 #pragma unroll
-      for (int kk = 0; kk < NKS; ++kk) qa[kk][2] = qa[kk][3] = 0u;
-      if (r_hi < R) {
-        const uint32_t* qp = reinterpret_cast<const uint32_t*>(q + row_of(r_hi) * D);
+    for (int kk = 0; kk < NKS; ++kk) qa[kk][2] = qa[kk][3] = 0u;
+    if (r_hi < R) {
+      const uint32_t* qp = reinterpret_cast<const uint32_t*>(q + row_of(r_hi) * D);
 #pragma unroll
-        for (int kk = 0; kk < NKS; ++kk) {
-          qa[kk][2] = __ldg(qp + kk * 8 + t);
-          qa[kk][3] = __ldg(qp + kk * 8 + 4 + t);
-        }
+      for (int kk = 0; kk < NKS; ++kk) {
+        qa[kk][2] = __ldg(qp + kk * 8 + t);
+        qa[kk][3] = __ldg(qp + kk * 8 + 4 + t);
       }
     }
   }
@@ -611,8 +585,8 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
       for (int kb = 0; kb < NKB; ++kb) {
         uint32_t b00, b01, b10, b11;
         ldsm_x4(kbase + sw_off<D>(kofs + kb * 16 + (mi >> 1) * 8 + ri, 2 * kk + (mi & 1)), b00, b01, b10, b11);
-        mma_rows<T, NA>(sc[2 * kb], qa[kk], b00, b01);
-        mma_rows<T, NA>(sc[2 * kb + 1], qa[kk], b10, b11);
+        Mma<T>::run(sc[2 * kb], qa[kk], b00, b01);
+        Mma<T>::run(sc[2 * kb + 1], qa[kk], b10, b11);
       }
     }
 
@@ -625,26 +599,21 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
         const int key = s0 + kofs + n * 8 + 2 * t + e;
         sc[n][e] = key < end_lo ? sc[n][e] * sl2 : -INFINITY;
         mx_lo = fmaxf(mx_lo, sc[n][e]);
-        if constexpr (NA == 4) {
-          sc[n][2 + e] = key < end_hi ? sc[n][2 + e] * sl2 : -INFINITY;
-          mx_hi = fmaxf(mx_hi, sc[n][2 + e]);
-        }
+        sc[n][2 + e] = key < end_hi ? sc[n][2 + e] * sl2 : -INFINITY;
+        mx_hi = fmaxf(mx_hi, sc[n][2 + e]);
       }
     mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
     mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-    const float mn_lo = fmaxf(m_lo, mx_lo);
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+    // a row that has seen no key yet keeps O = 0 and needs no rescale (alpha 1)
+    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
     const float mu_lo = (mn_lo == -INFINITY) ? 0.f : mn_lo;
-    const float al_lo = ex2f(m_lo - mu_lo);
+    const float mu_hi = (mn_hi == -INFINITY) ? 0.f : mn_hi;
+    const float al_lo = (mn_lo == -INFINITY) ? 1.f : ex2f(m_lo - mu_lo);
+    const float al_hi = (mn_hi == -INFINITY) ? 1.f : ex2f(m_hi - mu_hi);
     m_lo = mn_lo;
-    float mu_hi = 0.f, al_hi = 1.f;
-    if constexpr (NA == 4) {
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-      const float mn_hi = fmaxf(m_hi, mx_hi);
-      mu_hi = (mn_hi == -INFINITY) ? 0.f : mn_hi;
-      al_hi = ex2f(m_hi - mu_hi);
-      m_hi = mn_hi;
-    }
+    m_hi = mn_hi;
     float ps_lo = 0.f, ps_hi = 0.f;
 #pragma unroll
     for (int n = 0; n < 2 * NKB; ++n)
@@ -652,10 +621,8 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
       for (int e = 0; e < 2; ++e) {
         sc[n][e] = ex2f(sc[n][e] - mu_lo);
         ps_lo += sc[n][e];
-        if constexpr (NA == 4) {
-          sc[n][2 + e] = ex2f(sc[n][2 + e] - mu_hi);
-          ps_hi += sc[n][2 + e];
-        }
+        sc[n][2 + e] = ex2f(sc[n][2 + e] - mu_hi);
+        ps_hi += sc[n][2 + e];
       }
     l_lo = l_lo * al_lo + ps_lo;
     l_hi = l_hi * al_hi + ps_hi;
@@ -664,10 +631,8 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
       for (int n = 0; n < NNT; ++n) {
         o[n][0] *= al_lo;
         o[n][1] *= al_lo;
-        if constexpr (NA == 4) {
-          o[n][2] *= al_hi;
-          o[n][3] *= al_hi;
-        }
+        o[n][2] *= al_hi;
+        o[n][3] *= al_hi;
       }
     }
 
@@ -708,11 +673,11 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
         v1 &= mhi;
         v2 &= mlo;
         v3 &= mhi;
-        mma_rows<T, NA>(o[2 * dp], pa[kb], v0, v1);
-        mma_rows<T, NA>(o[2 * dp + 1], pa[kb], v2, v3);
+        Mma<T>::run(o[2 * dp], pa[kb], v0, v1);
+        Mma<T>::run(o[2 * dp + 1], pa[kb], v2, v3);
         if (split_p) {
-          mma_rows<T, NA>(o[2 * dp], la[kb], v0, v1);
-          mma_rows<T, NA>(o[2 * dp + 1], la[kb], v2, v3);
+          Mma<T>::run(o[2 * dp], la[kb], v0, v1);
+          Mma<T>::run(o[2 * dp + 1], la[kb], v2, v3);
         }
       }
     }
@@ -732,17 +697,13 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
 #pragma unroll
   for (int n = 0; n < NNT; ++n) {
     *reinterpret_cast<float2*>(&comb_o[(warp * 16 + g) * D + n * 8 + 2 * t]) = make_float2(o[n][0], o[n][1]);
-    if constexpr (NA == 4)
-      *reinterpret_cast<float2*>(&comb_o[(warp * 16 + g + 8) * D + n * 8 + 2 * t]) =
-          make_float2(o[n][2], o[n][3]);
+    *reinterpret_cast<float2*>(&comb_o[(warp * 16 + g + 8) * D + n * 8 + 2 * t]) = make_float2(o[n][2], o[n][3]);
   }
   if (t == 0) {
     comb_m[warp * 16 + g] = m_lo;
     comb_l[warp * 16 + g] = l_lo;
-    if constexpr (NA == 4) {
-      comb_m[warp * 16 + g + 8] = m_hi;
-      comb_l[warp * 16 + g + 8] = l_hi;
-    }
+    comb_m[warp * 16 + g + 8] = m_hi;
+    comb_l[warp * 16 + g + 8] = l_hi;
   }
   asm volatile("bar.sync 2, 128;" ::: "memory");
   if (*abort_flag) return;

@@ -297,3 +297,14 @@ def test_single_key_and_constant_v():
     w.kv_cache[:, 1] = c
     out, lse, _ = run(w)
     assert np.allclose(out, np.broadcast_to(c.double().numpy(), out.shape), atol=1e-2, rtol=0)
+
+
+def test_many_splits_merge():
+    """A 64-row small-query request cut into 400 splits (page_size 1, so the
+    cp.async path), merged by the merge kernel."""
+    w = workloads.make_custom("many", [8], [6400], 16, 2, 128, 1, dtype=torch.bfloat16, seed=22)
+    ro, rl = A.attention(w)
+    out, lse, plan = run(w, decode_chunk_pages=16)
+    h = plan_ref.decode_header(plan.dump())
+    assert h["n_dec"] == 2 * 400 and h["dec_class_items"] == [0, 0, 0, 800]
+    assert_close(out, lse, ro, rl, w.dtype, what="400 splits")
