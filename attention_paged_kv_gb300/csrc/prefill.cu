@@ -20,6 +20,9 @@
 //              cache, 128-byte swizzle), or cp.async for pages of < 8 slots.
 //   warp 9     MMA issuer (one thread) and TMEM owner.
 //
+// K and V tiles have separate two-slot rings (four for head_dim 64), so the
+// next K tile loads as soon as both S MMAs have read the slot it reuses.
+//
 // TMEM (512 columns): S_A at 0, S_B at 128 (fp32 128x128), O_A at 256, O_B at
 // 384 (fp32 128xD).  P (fp16/bf16, two per column) is written over the first
 // 64 columns of its S and feeds the PV MMA as a TMEM A operand.
@@ -39,6 +42,7 @@
 // (shared memory) and PV is issued for both, which gives P about 16 mantissa
 // bits where it matters.
 #include <cstring>
+#include <type_traits>
 
 #include "common.cuh"
 #include "internal.h"
@@ -75,6 +79,35 @@ __device__ __forceinline__ float ex2(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+
+// 2^x for a pair of x <= 0 on the FMA and integer pipes, to take part of the
+// softmax's exponentials off the multi-function unit (one row of S needs 128
+// of them; that unit does 4 a clock per SM sub-partition).  Cody-Waite range
+// reduction: x = r + f with r = round(x) (read off the mantissa of x + 1.5 *
+// 2^23) and f in [-1/2, 1/2]; 2^f from a cubic fitted to it on that interval
+// by iterated reweighted least squares (relative error below 7.5e-5, 2^-13.7;
+// exp2_poly_fit.py beside this file derives the coefficients); 2^r is added
+// to the exponent field.  x is clamped at -125 first so the exponent stays
+// normal: a masked key (x = -inf) yields about 2e-38 instead of 0.
+constexpr float kExp2C0 = 0.9999280571937561f, kExp2C1 = 0.6932609677314758f;
+constexpr float kExp2C2 = 0.2426111400127411f, kExp2C3 = 0.0551716685295105f;
+__device__ __forceinline__ float2 exp2_fma2(float2 x) {
+  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
+  x.x = fmaxf(x.x, -125.f);
+  x.y = fmaxf(x.y, -125.f);
+  const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
+  const float2 r = __fadd2_rn(t, make_float2(-kRound, -kRound));
+  const float2 f = __ffma2_rn(r, make_float2(-1.f, -1.f), x);
+  float2 q = __ffma2_rn(f, make_float2(kExp2C3, kExp2C3), make_float2(kExp2C2, kExp2C2));
+  q = __ffma2_rn(q, f, make_float2(kExp2C1, kExp2C1));
+  q = __ffma2_rn(q, f, make_float2(kExp2C0, kExp2C0));
+  return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(t.x) << 23)),
+                     __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(t.y) << 23)));
+}
+
+// Which pairs of each 32-column chunk take the polynomial: 6 of 16 (3/8 of
+// the exponentials), which balances the multi-function unit against issue.
+__device__ __forceinline__ constexpr bool poly_pair(int i) { return (i & 7) == 0 || (i & 7) == 3 || (i & 7) == 6; }
 
 // Bounded wait, made uniform across the warp (all lanes leave together).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
@@ -117,14 +150,18 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   auto plo_off = [&](int x) { return x == 0 ? C::OFF_PLO_A : C::OFF_PLO_B; };
 
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* full = bars;                // [NST] K/V tile landed
-  uint64_t* empty = bars + NST;         // [NST] both PV MMAs done with the stage
-  uint64_t* q_full = bars + 2 * NST;    // both Q tiles landed
+  // K and V have their own stages: a K slot is free once both S MMAs have
+  // read it, long before the PV MMAs are done with the V of the same tile
+  uint64_t* full_k = bars;              // [NST] K tile landed
+  uint64_t* full_v = bars + NST;        // [NST] V tile landed
+  uint64_t* empty_k = bars + 2 * NST;   // [NST] both S MMAs done with the K slot
+  uint64_t* empty_v = bars + 3 * NST;   // [NST] both PV MMAs done with the V slot
+  uint64_t* q_full = bars + 4 * NST;    // both Q tiles landed
   uint64_t* s_full = q_full + 1;        // [2] S_x MMA done
   uint64_t* p_full = s_full + 2;        // [2] P_x (and O_x correction) written
   uint64_t* o_done = p_full + 2;        // [2] PV_x MMA done
   uint64_t* fin = o_done + 2;           // all MMAs retired (teardown)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -140,8 +177,10 @@ __global__ void __launch_bounds__(kPreThreads, 1)
 
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], use_tma ? 1 : 32);
-      mbar_init(&empty[i], 1);
+      mbar_init(&full_k[i], use_tma ? 1 : 32);
+      mbar_init(&full_v[i], use_tma ? 1 : 32);
+      mbar_init(&empty_k[i], 1);
+      mbar_init(&empty_v[i], 1);
     }
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
@@ -174,77 +213,80 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       }
     }
     const int ps = p.ps, sh = p.ps_shift;
-    int issued = 0;
+    // tile j: K into slot j % NST once S_A(j - NST), S_B(j - NST) are done with
+    // it, then V once PV_A(j - NST), PV_B(j - NST) are
+    int issued_k = 0, issued_v = 0;
     for (int j = 0; j < nkt; ++j) {
       const int st = j % NST;
-      if (j >= NST) {
-        bool ok = true;
-        if (lane == 0) ok = mbar_wait(&empty[st], ((j / NST) - 1) & 1, abort_flag, p.status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!ok) break;
-      }
       const int k0 = it.kv_tok0 + j * kKvTile;
       const int kend = min(k0 + kKvTile, it.kv_tok1);
-      if (use_tma) {
-        const int pg0 = k0 >> sh;
-        const int npg = ((kend - 1) >> sh) - pg0 + 1;
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(npg * ps * 128 * NKB * 2));
-        __syncwarp();
-        for (int l = lane; l < npg; l += 32) {
-          const KvLoc loc = kv_locate(p.pages, rq.page_start, k0 + l * ps, sh);
-          int pid = loc.page;
-          if (static_cast<unsigned>(pid) >= static_cast<unsigned>(p.num_pages)) {
-            atomicOr(p.status, PA_DEV_BAD_INDEX);
-            pid = 0;
-          }
-#pragma unroll
-          for (int kb = 0; kb < NKB; ++kb) {
-            tma_load_4d(k_addr(st) + kb * C::BLK + l * ps * 128, &kv_map, kb * 64, it.kv_head, 0, 2 * pid,
-                        &full[st]);
-            tma_load_4d(v_addr(st) + kb * C::BLK + l * ps * 128, &kv_map, kb * 64, it.kv_head, 0, 2 * pid + 1,
-                        &full[st]);
-          }
+      bool ok = true;
+      for (int half = 0; half < 2 && ok; ++half) {  // 0: K, 1: V
+        uint64_t* empty = half ? empty_v : empty_k;
+        uint64_t* full = half ? full_v : full_k;
+        const uint32_t dst0 = half ? v_addr(st) : k_addr(st);
+        if (j >= NST) {
+          if (lane == 0) ok = mbar_wait(&empty[st], ((j / NST) - 1) & 1, abort_flag, p.status);
+          ok = __shfl_sync(0xffffffffu, ok, 0);
+          if (!ok) break;
         }
-      } else {
-        const T* kvb = static_cast<const T*>(p.kv);
-        for (int t = lane; t < kKvTile; t += 32) {
-          const int tok = k0 + t;
-          const bool valid = tok < kend;
-          const T* srck = kvb;
-          const T* srcv = kvb;
-          if (valid) {
-            const KvLoc loc = kv_locate(p.pages, rq.page_start, tok, sh);
+        if (use_tma) {
+          const int pg0 = k0 >> sh;
+          const int npg = ((kend - 1) >> sh) - pg0 + 1;
+          if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(npg * ps * 128 * NKB));
+          __syncwarp();
+          for (int l = lane; l < npg; l += 32) {
+            const KvLoc loc = kv_locate(p.pages, rq.page_start, k0 + l * ps, sh);
             int pid = loc.page;
             if (static_cast<unsigned>(pid) >= static_cast<unsigned>(p.num_pages)) {
               atomicOr(p.status, PA_DEV_BAD_INDEX);
               pid = 0;
             }
-            const size_t rowk = ((size_t(pid) * 2 * ps + loc.slot) * p.Hkv + it.kv_head) * D;
-            srck = kvb + rowk;
-            srcv = kvb + rowk + size_t(ps) * p.Hkv * D;
+#pragma unroll
+            for (int kb = 0; kb < NKB; ++kb)
+              tma_load_4d(dst0 + kb * C::BLK + l * ps * 128, &kv_map, kb * 64, it.kv_head, 0, 2 * pid + half,
+                          &full[st]);
           }
+        } else {
+          const T* kvb = static_cast<const T*>(p.kv);
+          for (int t = lane; t < kKvTile; t += 32) {
+            const int tok = k0 + t;
+            const bool valid = tok < kend;
+            const T* src = kvb;
+            if (valid) {
+              const KvLoc loc = kv_locate(p.pages, rq.page_start, tok, sh);
+              int pid = loc.page;
+              if (static_cast<unsigned>(pid) >= static_cast<unsigned>(p.num_pages)) {
+                atomicOr(p.status, PA_DEV_BAD_INDEX);
+                pid = 0;
+              }
+              src = kvb + ((size_t(pid) * 2 * ps + size_t(half) * ps + loc.slot) * p.Hkv + it.kv_head) * D;
+            }
 #pragma unroll
-          for (int kb = 0; kb < NKB; ++kb) {
+            for (int kb = 0; kb < NKB; ++kb) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const uint32_t off = kb * C::BLK + t * 128 + ((c ^ (t & 7)) * 16);
-              cp_async16(k_addr(st) + off, srck + (valid ? kb * 64 + c * 8 : 0), valid ? 16u : 0u);
-              cp_async16(v_addr(st) + off, srcv + (valid ? kb * 64 + c * 8 : 0), valid ? 16u : 0u);
+              for (int c = 0; c < 8; ++c) {
+                const uint32_t off = kb * C::BLK + t * 128 + ((c ^ (t & 7)) * 16);
+                cp_async16(dst0 + off, src + (valid ? kb * 64 + c * 8 : 0), valid ? 16u : 0u);
+              }
             }
           }
+          cp_async_commit();
+          cp_async_wait_all();
+          fence_proxy_async_smem();
+          mbar_arrive(&full[st]);
         }
-        cp_async_commit();
-        cp_async_wait_all();
-        fence_proxy_async_smem();
-        mbar_arrive(&full[st]);
+        if (half) issued_v = j + 1; else issued_k = j + 1;
       }
-      issued = j + 1;
+      if (!ok) break;
     }
     // drain: copies still in flight must land before the CTA's memory goes away
     if (lane == 0) {
       drain_wait(q_full, 0);
-      if (use_tma)
-        for (int j = max(0, issued - NST); j < issued; ++j) drain_wait(&full[j % NST], (j / NST) & 1);
+      if (use_tma) {
+        for (int j = max(0, issued_k - NST); j < issued_k; ++j) drain_wait(&full_k[j % NST], (j / NST) & 1);
+        for (int j = max(0, issued_v - NST); j < issued_v; ++j) drain_wait(&full_v[j % NST], (j / NST) & 1);
+      }
     }
     __syncwarp();
   } else if (warp == 9) {
@@ -279,26 +321,33 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         }
         tc_commit(&o_done[x]);
       };
+      // tile A's P_lo of the first key tile may live in K slot 0: then that
+      // slot is released only once PV_A(0) has read it
+      const bool plo_in_k = lo_split0 && (C::OFF_PLO_A == C::OFF_K);
       bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
-      if (ok) ok = mbar_wait(&full[0], 0, abort_flag, p.status);
+      if (ok) ok = mbar_wait(&full_k[0], 0, abort_flag, p.status);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
         if (has_b) issue_s(1, 0);
+        if (!plo_in_k) tc_commit(&empty_k[0]);
       }
       for (int j = 0; ok && j < nkt; ++j) {
         const int st = j % NST;
         const bool more = j + 1 < nkt;
         const int st1 = (j + 1) % NST;
         ok = mbar_wait(&p_full[0], j & 1, abort_flag, p.status);
+        if (ok) ok = mbar_wait(&full_v[st], (j / NST) & 1, abort_flag, p.status);
         if (!ok) break;
         tc_fence_after();
         issue_pv(0, j, st);
+        if (j == 0 && plo_in_k) tc_commit(&empty_k[0]);
         if (more) {
-          ok = mbar_wait(&full[st1], ((j + 1) / NST) & 1, abort_flag, p.status);
+          ok = mbar_wait(&full_k[st1], ((j + 1) / NST) & 1, abort_flag, p.status);
           if (!ok) break;
           tc_fence_after();
           issue_s(0, st1);
+          if (!has_b) tc_commit(&empty_k[st1]);
         }
         if (has_b) {
           ok = mbar_wait(&p_full[1], j & 1, abort_flag, p.status);
@@ -306,8 +355,11 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           tc_fence_after();
           issue_pv(1, j, st);
         }
-        tc_commit(&empty[st]);
-        if (has_b && more) issue_s(1, st1);
+        tc_commit(&empty_v[st]);
+        if (has_b && more) {
+          issue_s(1, st1);
+          tc_commit(&empty_k[st1]);
+        }
       }
       tc_commit(fin);
       drain_wait(fin, 0);
@@ -376,37 +428,53 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         if (!ok) break;
       }
 
-      // p = exp2(s * scale_log2 - m), row sum, P (hi) into TMEM over S
+      // p = exp2(s * scale_log2 - m), row sum, P (hi) into TMEM over S.  The
+      // first key tile of a sequence (P split into hi + lo) takes every
+      // exponential from the multi-function unit; the others send 3/8 of them
+      // through exp2_fma2.
       const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
-      float2 acc2 = make_float2(0.f, 0.f);
+      auto softmax_p = [&](auto poly_tag) -> float {
+        constexpr bool kPoly = decltype(poly_tag)::value;
+        float2 acc2 = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t ph[16];
+        for (int c = 0; c < 4; ++c) {
+          uint32_t ph[16];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint32_t lw[4];
+          for (int u = 0; u < 4; ++u) {
+            uint32_t lw[4];
 #pragma unroll
-          for (int v = 0; v < 4; ++v) {
-            const int i = 4 * u + v, k = 32 * c + 2 * i;
-            const float2 t2 = __ffma2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), sc2, nm2);
-            const float a = ex2(t2.x), b = ex2(t2.y);
-            acc2 = __fadd2_rn(acc2, make_float2(a, b));
-            ph[i] = Elt<T>::from_f2(a, b);
-            if (lo_split) {
-              const float2 hi = Elt<T>::to_f2(ph[i]);
-              lw[v] = Elt<T>::from_f2(a - hi.x, b - hi.y);
+            for (int v = 0; v < 4; ++v) {
+              const int i = 4 * u + v, k = 32 * c + 2 * i;
+              const float2 t2 =
+                  __ffma2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), sc2, nm2);
+              float a, b;
+              if (kPoly && poly_pair(i)) {
+                const float2 e = exp2_fma2(t2);
+                a = e.x;
+                b = e.y;
+              } else {
+                a = ex2(t2.x);
+                b = ex2(t2.y);
+              }
+              acc2 = __fadd2_rn(acc2, make_float2(a, b));
+              ph[i] = Elt<T>::from_f2(a, b);
+              if (!kPoly && lo_split) {
+                const float2 hi = Elt<T>::to_f2(ph[i]);
+                lw[v] = Elt<T>::from_f2(a - hi.x, b - hi.y);
+              }
+            }
+            if (!kPoly && lo_split) {
+              // keys 32c + 8u .. +7 of row r -> K-major 128-byte-swizzled smem
+              const int cc = (c & 1) * 4 + u;
+              *reinterpret_cast<uint4*>(smem + plo_off(x) + (c >> 1) * C::BLK + r * 128 + ((cc ^ (r & 7)) * 16)) =
+                  make_uint4(lw[0], lw[1], lw[2], lw[3]);
             }
           }
-          if (lo_split) {
-            // keys 32c + 8u .. +7 of row r -> K-major 128-byte-swizzled smem
-            const int cc = (c & 1) * 4 + u;
-            *reinterpret_cast<uint4*>(smem + plo_off(x) + (c >> 1) * C::BLK + r * 128 + ((cc ^ (r & 7)) * 16)) =
-                make_uint4(lw[0], lw[1], lw[2], lw[3]);
-          }
+          tmem_st16(s_col + c * 16, ph);
         }
-        tmem_st16(s_col + c * 16, ph);
-      }
-      const float rs = acc2.x + acc2.y;
+        return acc2.x + acc2.y;
+      };
+      const float rs = (j == 0) ? softmax_p(std::false_type{}) : softmax_p(std::true_type{});
       // S_x(j) done implies PV_x(j-1) done (the MMAs run in issue order); the
       // barrier makes O's contents visible before it is rescaled
       // PV of the previous tile must be done before O is rescaled
@@ -432,7 +500,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         const int valid = it.kv_tok1 - k0;
         if (valid < kKvTile) {
           const int st = j % NST;
-          ok = warp_wait(&full[st], (j / NST) & 1, abort_flag, p.status);
+          ok = warp_wait(&full_v[st], (j / NST) & 1, abort_flag, p.status);
           if (!ok) break;
           if (r >= valid) {
             uint8_t* vrow = smem + C::OFF_V + st * C::KV_BYTES + r * 128;
