@@ -11,7 +11,9 @@
 //  2. Small-query requests go to the decode kernels: with group size
 //     G = Hq/Hkv in {1, 2, 4, 8, 16}, a request whose R_b = qo_b * G packed
 //     (token, head) rows number at most 64 (one decoded token, or a few
-//     speculative ones), unless force_prefill.  With decode_cuda_cores only
+//     speculative ones) and, when qo_b > 1, that has more keys than one
+//     prefill key tile (kv_b > 128; a shorter one costs the prefill kernel
+//     a single key tile), unless force_prefill.  With decode_cuda_cores only
 //     qo_b == 1 at G <= 8 qualifies (the CUDA-core kernel's shapes).  Every
 //     other request with rows -> tensor-core prefill.  The decode items run
 //     on the CUDA-core kernel when decode_cuda_cores is set, or when G <= 2
@@ -124,7 +126,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   bool multi_tok = false;
   for (int b = 0; b < B; ++b) {
     const int64_t qo = req[b].qo;
-    bool d = qo >= 1 && dec_group && !in.force_prefill && qo * G <= kDecMaxRows;
+    bool d = qo >= 1 && dec_group && !in.force_prefill && qo * G <= kDecMaxRows && (qo == 1 || req[b].kv > kKvTile);
     if (in.decode_cuda_cores) d = d && qo == 1 && G <= 8;
     is_dec[b] = d ? 1 : 0;
     if (d && qo > 1) multi_tok = true;

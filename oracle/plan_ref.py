@@ -14,7 +14,8 @@ Rules (the planner is deterministic; nothing depends on timing):
    (see ``oracle.attention.kv_len_of``), page_start_b.
 2. Small-query requests go to the decode kernels: G = Hq/Hkv is one of
    1, 2, 4, 8, 16, the request's R_b = qo_b * G packed (token, head) rows
-   number at most 64, and ``force_prefill`` is off.  With
+   number at most 64, a request with qo_b > 1 has kv_b > 128 (more keys
+   than one prefill key tile), and ``force_prefill`` is off.  With
    ``decode_cuda_cores`` only qo_b == 1 at G <= 8 qualifies.  Every other
    request with qo_b >= 1 goes to the tensor-core prefill kernel.  The
    decode items run on CUDA cores (header word 29 = 1) when
@@ -137,8 +138,9 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
     T = int(np.asarray(qo_indptr)[-1])
 
     is_dec = []
-    for (qo, _, _, _) in lens:
-        d = qo >= 1 and G in DECODE_GROUPS and not force_prefill and qo * G <= DEC_MAX_ROWS
+    for (qo, kv, _, _) in lens:
+        d = (qo >= 1 and G in DECODE_GROUPS and not force_prefill and qo * G <= DEC_MAX_ROWS
+             and (qo == 1 or kv > KV_TILE))
         if decode_cuda_cores:
             d = d and qo == 1 and G <= 8
         is_dec.append(d)

@@ -63,8 +63,8 @@ def test_nan_outside_the_kv_range(opts, ps):
     """Slots past each request's last_page_len and pages no request uses
     hold NaN: no kernel may let them reach an output (masked keys still
     meet V in the P V product, where 0 * NaN would be NaN)."""
-    lens = [1, 63, 64, 65, 127, 129, 200, 1000, 100, 300]
-    qo = [1, 1, 2, 4, 8, 1, 1, 1, 40, 130]  # 2, 4, 8 tokens x 8 heads: small-query items
+    lens = [1, 63, 64, 65, 127, 129, 200, 1000, 100, 300, 129, 300, 500]
+    qo = [1] * 8 + [40, 130] + [2, 4, 8]  # the last three: 2, 4, 8 tokens x 8 heads, small-query items
     w = workloads.make_custom("nan", qo, lens, 16, 2, 128, ps, dtype=torch.bfloat16, seed=ps + 3, extra_pages=5)
     used = torch.zeros(w.num_pages, dtype=torch.bool)
     kv = w.kv_cache.clone()
@@ -219,11 +219,12 @@ SMALLQ = [(1, [64, 2, 9, 1, 33]), (2, [1, 4, 8, 16, 32]), (4, [2, 3, 4, 8, 16]),
 @pytest.mark.parametrize("G,qos", SMALLQ, ids=[f"G{g}" for g, _ in SMALLQ])
 @pytest.mark.parametrize("opts", [{}, {"decode_chunk_pages": 2}], ids=["whole", "split"])
 def test_small_query(dtype, G, qos, opts):
-    """Requests of a few query tokens (qo_len * G <= 64 packed rows) on the
-    warp-MMA kernel: every row class, kv_len from qo_len (row 0 sees one
-    key) to past 512, each row with its own causal limit."""
-    extra = [0, 5, 63, 130, 700]
-    kvs = [q + e for q, e in zip(qos, extra)]
+    """Requests of a few query tokens (qo_len * G <= 64 packed rows, more
+    than 128 keys when qo_len > 1) on the warp-MMA kernel: every row class,
+    one-token requests from a single key up, each row with its own causal
+    limit."""
+    extra = [129, 135, 200, 300, 700]
+    kvs = [(1 if q == 1 and i == 0 else q + e) for i, (q, e) in enumerate(zip(qos, extra))]
     w = workloads.make_custom("sq", qos, kvs, G * 2, 2, 128, 16, dtype=dtype, seed=G * 7 + len(opts))
     ro, rl = A.attention(w)
     out, lse, plan = run(w, **opts)
@@ -236,7 +237,7 @@ def test_small_query(dtype, G, qos, opts):
 def test_small_query_layouts(D, ps, causal):
     """Small-query items at head_dim 64, TMA page rows (64) and cp.async
     pages (1, 4 slots), and without the causal mask."""
-    qos, kvs = [8, 3, 1, 5], [8, 70, 300, 1200]
+    qos, kvs = [8, 3, 1, 5], [200, 170, 300, 1200]
     w = workloads.make_custom("sql", qos, kvs, 16, 2, D, ps, dtype=torch.bfloat16, causal=causal, seed=D + ps)
     ro, rl = A.attention(w)
     for opts in ({}, {"decode_chunk_pages": max(1, 128 // ps)}):
@@ -248,7 +249,7 @@ def test_small_query_layouts(D, ps, causal):
 def test_small_query_equals_prefill_kernel():
     """The speculative-decoding shape on both kernels (atol = rtol = 1e-3 in
     fp16), the small-query analogue of the timing script's closing check."""
-    w = workloads.make_custom("sqp", [4] * 12, [40 * i + 4 for i in range(12)], 32, 4, 128, 16, seed=9)
+    w = workloads.make_custom("sqp", [4] * 12, [40 * i + 130 for i in range(12)], 32, 4, 128, 16, seed=9)
     o1, l1, p1 = run(w)
     o2, l2, p2 = run(w, force_prefill=True)
     assert plan_ref.decode_header(p1.dump())["n_pre"] == 0 and plan_ref.decode_header(p2.dump())["n_dec"] == 0

@@ -213,7 +213,7 @@ def test_plan_small_query_semantics(lib):
     """Requests of a few query tokens (qo_len * G <= 64 packed rows) become
     small-query items of the decode kernels, grouped by row class; their
     split groups merge per (token, kv head) with a stride of qo_len * G."""
-    w = workloads.mixed(num_decode=24, prefill_len=0, kv_lo=16, kv_hi=3000, decode_qo=4)
+    w = workloads.mixed(num_decode=24, prefill_len=0, kv_lo=200, kv_hi=3000, decode_qo=4)
     blob = _lib_blob(w, num_sms=148, decode_chunk_pages=16)
     h = plan_ref.decode_header(blob)
     dec, pre, mer = plan_ref.items(blob)
@@ -228,7 +228,10 @@ def test_plan_small_query_semantics(lib):
     # G <= 2 with single-token requests only: CUDA cores; one two-token request moves all to MMA
     a = workloads.make_custom("g2", [1, 1, 1], [10, 20, 30], 4, 2, 64, 4, seed=1)
     assert plan_ref.decode_header(_lib_blob(a, num_sms=148))["dec_cuda_cores"] == 1
-    b = workloads.make_custom("g2", [1, 2, 1], [10, 20, 30], 4, 2, 64, 4, seed=1)
+    b = workloads.make_custom("g2", [1, 2, 1], [10, 200, 30], 4, 2, 64, 4, seed=1)
+    c = workloads.make_custom("g2", [1, 2, 1], [10, 20, 30], 4, 2, 64, 4, seed=1)  # 2 tokens, 20 keys: prefill
+    hc = plan_ref.decode_header(_lib_blob(c, num_sms=148))
+    assert hc["dec_cuda_cores"] == 1 and hc["n_pre"] > 0
     hb = plan_ref.decode_header(_lib_blob(b, num_sms=148))
     assert hb["dec_cuda_cores"] == 0 and hb["n_pre"] == 0 and hb["dec_class_items"][0] == hb["n_dec"]
 
