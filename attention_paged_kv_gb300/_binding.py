@@ -57,7 +57,7 @@ class Options(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int32), ("force_prefill", ctypes.c_int32),
                 ("decode_chunk_pages", ctypes.c_int32), ("prefill_chunk_tiles", ctypes.c_int32),
                 ("force_cp_async", ctypes.c_int32), ("decode_cuda_cores", ctypes.c_int32),
-                ("reserved", ctypes.c_int32 * 2)]
+                ("kv_layout", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
@@ -136,8 +136,21 @@ def dtype_code(dtype) -> int:
     raise PagedAttnError(PA_ERR_UNSUPPORTED, f"dtype {dtype}")
 
 
+PA_LAYOUT_NHD = 0
+PA_LAYOUT_HND = 1
+
+
+def layout_code(layout) -> int:
+    """"NHD" / "HND" (or the PA_LAYOUT_* codes) -> code."""
+    if layout in ("NHD", "nhd", PA_LAYOUT_NHD):
+        return PA_LAYOUT_NHD
+    if layout in ("HND", "hnd", PA_LAYOUT_HND):
+        return PA_LAYOUT_HND
+    raise PagedAttnError(PA_ERR_UNSUPPORTED, f"kv_layout {layout!r}")
+
+
 def _options(num_sms=0, force_prefill=False, decode_chunk_pages=0, prefill_chunk_tiles=0,
-             force_cp_async=False, decode_cuda_cores=False) -> Options:
+             force_cp_async=False, decode_cuda_cores=False, kv_layout="NHD") -> Options:
     o = Options()
     o.num_sms = int(num_sms)
     o.force_prefill = int(bool(force_prefill))
@@ -145,6 +158,7 @@ def _options(num_sms=0, force_prefill=False, decode_chunk_pages=0, prefill_chunk
     o.prefill_chunk_tiles = int(prefill_chunk_tiles)
     o.force_cp_async = int(bool(force_cp_async))
     o.decode_cuda_cores = int(bool(decode_cuda_cores))
+    o.kv_layout = layout_code(kv_layout)
     return o
 
 
@@ -185,6 +199,7 @@ class Plan:
         self.num_qo_heads, self.num_kv_heads = int(num_qo_heads), int(num_kv_heads)
         self.head_dim, self.page_size, self.num_pages = int(head_dim), int(page_size), int(num_pages)
         self.dtype_code = dtype_code(dtype)
+        self.kv_layout = layout_code(opts.get("kv_layout", "NHD"))
         self.causal = bool(causal)
         arrs = [_i32(x) for x in (qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len)]
         if len(arrs[0]) < 1:
@@ -226,7 +241,8 @@ class Plan:
                 raise PagedAttnError(PA_ERR_INVALID_ARG, f"{name} dtype differs from the plan's")
         if tuple(q.shape) != (T, Hq, D) or tuple(out.shape) != (T, Hq, D):
             raise PagedAttnError(PA_ERR_INVALID_ARG, f"q/out must be [{T}, {Hq}, {D}]")
-        want_kv = (self.num_pages, 2, self.page_size, self.num_kv_heads, D)
+        want_kv = ((self.num_pages, 2, self.num_kv_heads, self.page_size, D) if self.kv_layout == PA_LAYOUT_HND
+                   else (self.num_pages, 2, self.page_size, self.num_kv_heads, D))
         if tuple(kv_cache.shape) != want_kv:
             raise PagedAttnError(PA_ERR_INVALID_ARG, f"kv_cache must be {list(want_kv)}")
         if lse is not None and (lse.dtype != torch.float32 or tuple(lse.shape) != (T, Hq) or not lse.is_contiguous()):

@@ -63,10 +63,13 @@ pagedattn_status encode_kv_map(CUtensorMap* m, const pa::HostPlan& hp, const voi
                                uint32_t box2, CUtensorMapSwizzle sw) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return set_err(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
-  const cuuint64_t dims[4] = {cuuint64_t(hp.D), cuuint64_t(hp.Hkv), cuuint64_t(hp.ps), cuuint64_t(2) * hp.num_pages};
-  const cuuint64_t strides[3] = {cuuint64_t(hp.D) * 2, cuuint64_t(hp.Hkv) * hp.D * 2,
-                                 cuuint64_t(hp.ps) * hp.Hkv * hp.D * 2};
-  const cuuint32_t box[4] = {box0, 1, box2, 1};
+  // NHD: (D, Hkv, ps, 2P); HND: (D, ps, Hkv, 2P) -- innermost first, so a
+  // box of rows of one head is {box0, 1, box2, 1} or {box0, box2, 1, 1}
+  const cuuint64_t mid1 = hp.hnd ? cuuint64_t(hp.ps) : cuuint64_t(hp.Hkv);
+  const cuuint64_t mid2 = hp.hnd ? cuuint64_t(hp.Hkv) : cuuint64_t(hp.ps);
+  const cuuint64_t dims[4] = {cuuint64_t(hp.D), mid1, mid2, cuuint64_t(2) * hp.num_pages};
+  const cuuint64_t strides[3] = {cuuint64_t(hp.D) * 2, mid1 * hp.D * 2, mid2 * mid1 * hp.D * 2};
+  const cuuint32_t box[4] = {box0, hp.hnd ? box2 : 1u, hp.hnd ? 1u : box2, 1};
   const cuuint32_t estr[4] = {1, 1, 1, 1};
   const CUtensorMapDataType dt =
       hp.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -119,8 +122,9 @@ pagedattn_status fill_inputs(pa::PlanInputs* in, const int32_t* qo_indptr, const
   pagedattn_options o;
   std::memset(&o, 0, sizeof(o));
   if (opts) o = *opts;
-  for (int i = 0; i < 2; ++i)
-    if (o.reserved[i] != 0) return set_err(PA_ERR_INVALID_ARG, "pagedattn_options.reserved must be zero");
+  if (o.reserved[0] != 0) return set_err(PA_ERR_INVALID_ARG, "pagedattn_options.reserved must be zero");
+  if (o.kv_layout != PA_LAYOUT_NHD && o.kv_layout != PA_LAYOUT_HND)
+    return set_err(PA_ERR_UNSUPPORTED, "kv_layout must be PA_LAYOUT_NHD or PA_LAYOUT_HND");
   if (o.num_sms < 0 || o.decode_chunk_pages < 0 || o.prefill_chunk_tiles < 0)
     return set_err(PA_ERR_INVALID_ARG, "negative option");
   in->num_sms = o.num_sms;
@@ -128,6 +132,7 @@ pagedattn_status fill_inputs(pa::PlanInputs* in, const int32_t* qo_indptr, const
   in->decode_chunk_pages = o.decode_chunk_pages;
   in->prefill_chunk_tiles = o.prefill_chunk_tiles;
   in->decode_cuda_cores = o.decode_cuda_cores ? 1 : 0;
+  in->kv_layout = o.kv_layout;
   if (in->num_sms == 0) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -174,6 +179,7 @@ KParams make_params(const RunArgs& a) {
   while ((1 << s) < hp.G) ++s;
   k.g_shift = s;
   k.causal = hp.causal;
+  k.hnd = hp.hnd;
   k.num_pages = hp.num_pages;
   k.scale_log2 = float(1.4426950408889634 / std::sqrt(double(hp.D)));
   return k;

@@ -34,6 +34,7 @@ struct KParams {
   float* part_lse;          // [n_part]
   int32_t* status;          // device status word
   int32_t Hq, Hkv, D, ps, ps_shift, G, g_shift, causal, num_pages, n_items;
+  int32_t hnd;              // cache layout: 0 NHD [P, 2, ps, Hkv, D], 1 HND [P, 2, Hkv, ps, D]
   float scale_log2;         // log2(e) / sqrt(D)
 };
 
@@ -122,6 +123,24 @@ __device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map
       " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(smem_u32(bar))
       : "memory");
+}
+
+// Element offset / D of the K (half 0) or V (half 1) row of (page, slot, kv
+// head) in the cache, for either layout.
+__device__ __forceinline__ size_t kv_row(const KParams& p, int pid, int half, int slot, int h) {
+  return p.hnd ? ((size_t(pid) * 2 + half) * p.Hkv + h) * p.ps + slot
+               : ((size_t(pid) * 2 + half) * p.ps + slot) * p.Hkv + h;
+}
+
+// TMA copy of page rows [slot, slot + box rows) of kv head h, page half z =
+// 2 * page + half, columns [c0, c0 + 64), through the 4-D cache map: (D, Hkv,
+// ps, 2P) for NHD, (D, ps, Hkv, 2P) for HND.
+__device__ __forceinline__ void tma_kv_rows(uint32_t dst, const CUtensorMap* map, int c0, int h, int slot, int z,
+                                            uint64_t* bar, int hnd) {
+  if (hnd)
+    tma_load_4d(dst, map, c0, slot, h, z, bar);
+  else
+    tma_load_4d(dst, map, c0, h, slot, z, bar);
 }
 
 // 3-D tiled TMA load global -> shared, completion counted on `bar` in bytes.

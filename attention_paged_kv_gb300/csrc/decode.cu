@@ -116,10 +116,10 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
           }
 #pragma unroll
           for (int kb = 0; kb < NKB; ++kb) {
-            tma_load_4d(kdst + kb * C::BLK + b * BR * 128, &kv_map, kb * 64, it.kv_head, loc.slot, 2 * pid,
-                        &full[st]);
-            tma_load_4d(kdst + C::STAGE_K + kb * C::BLK + b * BR * 128, &kv_map, kb * 64, it.kv_head, loc.slot,
-                        2 * pid + 1, &full[st]);
+            tma_kv_rows(kdst + kb * C::BLK + b * BR * 128, &kv_map, kb * 64, it.kv_head, loc.slot, 2 * pid,
+                        &full[st], p.hnd);
+            tma_kv_rows(kdst + C::STAGE_K + kb * C::BLK + b * BR * 128, &kv_map, kb * 64, it.kv_head, loc.slot,
+                        2 * pid + 1, &full[st], p.hnd);
           }
         }
       } else {
@@ -135,9 +135,8 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
               atomicOr(p.status, PA_DEV_BAD_INDEX);
               pid = 0;
             }
-            const size_t rowk = ((size_t(pid) * 2 * p.ps + loc.slot) * p.Hkv + it.kv_head) * D;
-            srck = kvb + rowk;
-            srcv = kvb + rowk + size_t(p.ps) * p.Hkv * D;
+            srck = kvb + kv_row(p, pid, 0, loc.slot, it.kv_head) * D;
+            srcv = kvb + kv_row(p, pid, 1, loc.slot, it.kv_head) * D;
           }
 #pragma unroll
           for (int c = 0; c < NCH; ++c) {

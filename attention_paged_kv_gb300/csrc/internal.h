@@ -20,6 +20,7 @@ struct HostPlan {
   int32_t B = 0, Hq = 0, Hkv = 0, D = 0, ps = 0, num_pages = 0, dtype = 0, causal = 1, T = 0, nnz = 0;
   int32_t n_dec = 0, n_pre = 0, n_merge = 0, n_part = 0, G = 1, num_sms = 0;
   int32_t dec_cores = 0;                  // 1: decode items run on the CUDA-core kernel
+  int32_t hnd = 0;                        // cache layout: 0 NHD, 1 HND
   int32_t n_dec_class[4] = {0, 0, 0, 0};  // decode items per row class, consecutive in item order
   size_t blob_bytes = 0, off_part_o = 0, off_part_lse = 0, total_bytes = 0;
   size_t off_pages = 0, off_req = 0, off_dec = 0, off_pre = 0, off_merge = 0;
@@ -32,7 +33,7 @@ struct PlanInputs {
   const int32_t* kv_page_indices;
   const int32_t* kv_last_page_len;
   int32_t B, Hq, Hkv, D, ps, num_pages, dtype, causal;
-  int32_t num_sms, force_prefill, decode_chunk_pages, prefill_chunk_tiles, decode_cuda_cores;
+  int32_t num_sms, force_prefill, decode_chunk_pages, prefill_chunk_tiles, decode_cuda_cores, kv_layout;
 };
 
 // Validate and partition; on failure returns the status and fills `err`.

@@ -254,6 +254,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
                          int32_t(off_part_lse), int32_t(total), dec_cores};
   std::memcpy(blob.data(), hdr, sizeof(hdr));
   for (int c = 0; c < kDecClasses; ++c) blob[H_NDEC_CLASS0 + c] = n_class[c];
+  blob[H_LAYOUT] = in.kv_layout;
   if (nnz) std::memcpy(blob.data() + off_pages / 4, in.kv_page_indices, size_t(4 * nnz));
   for (int b = 0; b < B; ++b) {
     int32_t* r = blob.data() + off_req / 4 + 4 * b;
@@ -281,6 +282,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   hp->n_dec = int32_t(dec.size()); hp->n_pre = int32_t(pre.size()); hp->n_merge = int32_t(merges.size());
   hp->n_part = int32_t(part); hp->G = G; hp->num_sms = in.num_sms;
   hp->dec_cores = dec_cores;
+  hp->hnd = in.kv_layout;
   for (int c = 0; c < kDecClasses; ++c) hp->n_dec_class[c] = n_class[c];
   hp->blob_bytes = size_t(blob_bytes); hp->off_part_o = size_t(off_part_o);
   hp->off_part_lse = size_t(off_part_lse); hp->total_bytes = size_t(total);

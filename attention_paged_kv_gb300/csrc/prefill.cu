@@ -244,8 +244,8 @@ __global__ void __launch_bounds__(kPreThreads, 1)
             }
 #pragma unroll
             for (int kb = 0; kb < NKB; ++kb)
-              tma_load_4d(dst0 + kb * C::BLK + l * ps * 128, &kv_map, kb * 64, it.kv_head, 0, 2 * pid + half,
-                          &full[st]);
+              tma_kv_rows(dst0 + kb * C::BLK + l * ps * 128, &kv_map, kb * 64, it.kv_head, 0, 2 * pid + half,
+                          &full[st], p.hnd);
           }
         } else {
           const T* kvb = static_cast<const T*>(p.kv);
@@ -260,7 +260,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
                 atomicOr(p.status, PA_DEV_BAD_INDEX);
                 pid = 0;
               }
-              src = kvb + ((size_t(pid) * 2 * ps + size_t(half) * ps + loc.slot) * p.Hkv + it.kv_head) * D;
+              src = kvb + kv_row(p, pid, half, loc.slot, it.kv_head) * D;
             }
 #pragma unroll
             for (int kb = 0; kb < NKB; ++kb) {

@@ -85,8 +85,21 @@ typedef struct {
                                   the CUDA-core decode kernel, and multi-token
                                   requests all go to the prefill kernel (default:
                                   the warp-MMA small-query kernel, see plan)        */
-  int32_t reserved[2];         /* must be 0                                          */
+  int32_t kv_layout;           /* PA_LAYOUT_NHD (default) or PA_LAYOUT_HND: see below */
+  int32_t reserved[1];         /* must be 0                                          */
 } pagedattn_options;
+
+/*
+ * Cache layouts (pagedattn_options.kv_layout).  Both hold, per physical page,
+ * the page_size K rows and then the page_size V rows of every kv head; the
+ * FlashInfer timing script passes "NHD" and the alternative it implies keeps
+ * each head's rows together:
+ *   PA_LAYOUT_NHD  kv_cache[num_pages][2][page_size][num_kv_heads][head_dim]
+ *   PA_LAYOUT_HND  kv_cache[num_pages][2][num_kv_heads][page_size][head_dim]
+ * The results are identical (bit for bit) for the same logical cache.
+ */
+#define PA_LAYOUT_NHD 0
+#define PA_LAYOUT_HND 1
 
 /* Stage bits for pagedattn_run_stages. */
 #define PA_STAGE_PREFILL 1u

@@ -61,7 +61,8 @@ start of the workspace:
                 n_part_rows, dec_chunk_pages, pre_chunk_tiles, num_sms, G,
                 off_pages, off_req, off_dec, off_pre, off_merge, blob_bytes,
                 off_part_o, off_part_lse, total_bytes, dec_cuda_cores, 0, 0,
-                [32] status word, [33..36] decode items per row class, 0...
+                [32] status word, [33..36] decode items per row class,
+                [37] cache layout (0 NHD, 1 HND), 0...
     pages[nnz]       copy of kv_page_indices
     req[B][4]        qo_start, qo_len, kv_len, page_start
     dec[n_dec][8]    req, kv_head, tok0, tok1, part_row(-1 = direct), 0, 0, 0
@@ -75,7 +76,7 @@ import numpy as np
 from .attention import PlanError, request_lengths
 
 MAGIC = 0x50414731
-VERSION = 2
+VERSION = 3
 HDR_WORDS = 64
 STATUS_WORD = 32
 Q_ROWS = 128       # packed query rows per prefill MMA tile (G must divide it)
@@ -107,7 +108,8 @@ def _align(x, a=256):
 
 def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_heads,
           num_kv_heads, head_dim, page_size, num_pages, dtype=BF16, causal=True, num_sms=148,
-          force_prefill=False, decode_chunk_pages=0, prefill_chunk_tiles=0, decode_cuda_cores=False):
+          force_prefill=False, decode_chunk_pages=0, prefill_chunk_tiles=0, decode_cuda_cores=False,
+          kv_layout="NHD"):
     """Return the metadata blob (np.int32) the planner must produce."""
     Hq, Hkv, D, ps = int(num_qo_heads), int(num_kv_heads), int(head_dim), int(page_size)
     if Hq < 1 or Hkv < 1 or Hq % Hkv:
@@ -232,6 +234,7 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
            off_part_lse, total, dec_cores]
     blob[:len(hdr)] = hdr
     blob[33:33 + len(n_class)] = n_class
+    blob[37] = {"NHD": 0, "HND": 1}[kv_layout] if isinstance(kv_layout, str) else int(kv_layout)
     blob[off_pages // 4: off_pages // 4 + nnz] = indices
     req = np.array([(int(qo_indptr[b]), qo, kv, p0) for b, (qo, kv, p0, _) in enumerate(lens)],
                    np.int32).reshape(-1, 4)

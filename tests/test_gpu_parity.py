@@ -309,3 +309,38 @@ def test_many_splits_merge():
     h = plan_ref.decode_header(plan.dump())
     assert h["n_dec"] == 2 * 400 and h["dec_class_items"] == [0, 0, 0, 800]
     assert_close(out, lse, ro, rl, w.dtype, what="400 splits")
+
+
+def _hnd(kv):
+    """The same logical cache in the HND layout [P, 2, Hkv, page_size, D]."""
+    return kv.permute(0, 1, 3, 2, 4).contiguous()
+
+
+HND_CASES = [("tiny", {}), ("tiny", {"force_prefill": True}), ("mixed", {}),
+             ("mixed", {"decode_chunk_pages": 1, "prefill_chunk_tiles": 1}), ("decode", {"decode_cuda_cores": True}),
+             ("smallq", {}), ("ps1", {}), ("ps128", {}), ("mixed", {"force_cp_async": True})]
+
+
+@pytest.mark.parametrize("name,opts", HND_CASES, ids=[f"{n}-{'-'.join(map(str, o))}" for n, o in HND_CASES])
+def test_hnd_layout_equals_nhd_bitexact(name, opts):
+    """The HND cache layout reads the same keys and values through other
+    addresses: every kernel path gives bit-identical results to NHD."""
+    if name == "tiny":
+        w = workloads.tiny()
+    elif name == "mixed":
+        w = workloads.mixed(num_decode=24, prefill_len=700, kv_lo=16, kv_hi=3000)
+    elif name == "decode":
+        w = workloads.decode(batch_size=16)
+    elif name == "smallq":
+        w = workloads.make_custom("hq", [4, 2, 8, 1], [300, 700, 200, 90], 16, 2, 128, 16, dtype=torch.bfloat16,
+                                  seed=31)
+    else:
+        ps = int(name[2:])
+        w = workloads.make_custom("hp", [1, 9, 1, 70], [77, 9, 300, 270], 8, 2, 128, ps, dtype=torch.bfloat16,
+                                  seed=ps + 40)
+    o1, l1, _ = run(w, **opts)
+    o2, l2, _ = run(w, kv=_hnd(w.kv_cache), kv_layout="HND", **opts)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    if name in ("tiny", "smallq"):
+        ro, rl = A.attention(w)
+        assert_close(o2, l2, ro, rl, w.dtype, what=f"HND {name}")

@@ -58,6 +58,7 @@ CASES = [
     ("random", {}), ("random_nc", {}), ("empty", {}), ("qo0", {}),
     ("random", {"decode_cuda_cores": True}), ("smallq", {}), ("smallq", {"decode_cuda_cores": True}),
     ("smallq", {"decode_chunk_pages": 2}), ("smallq_g16", {}), ("smallq_g1", {}), ("specdec", {}),
+    ("tiny", {"kv_layout": "HND"}), ("smallq", {"kv_layout": "HND"}),
 ]
 
 
@@ -177,10 +178,15 @@ def test_workspace_too_small_and_options(lib):
     st = lib.pagedattn_plan(*[x.ctypes.data_as(P) for x in a], 4, 2, 1, 64, 4, w.num_pages, 0, 1, fake, 64,
                             ctypes.byref(o), None, ctypes.byref(h))
     assert st == pa.PA_ERR_WORKSPACE_TOO_SMALL and not h.value
-    o.reserved[1] = 3
+    o.reserved[0] = 3
     st = lib.pagedattn_plan(*[x.ctypes.data_as(P) for x in a], 4, 2, 1, 64, 4, w.num_pages, 0, 1, None, 0,
                             ctypes.byref(o), None, ctypes.byref(h))
     assert st == pa.PA_ERR_INVALID_ARG
+    o.reserved[0] = 0
+    o.kv_layout = 2
+    st = lib.pagedattn_plan(*[x.ctypes.data_as(P) for x in a], 4, 2, 1, 64, 4, w.num_pages, 0, 1, None, 0,
+                            ctypes.byref(o), None, ctypes.byref(h))
+    assert st == pa.PA_ERR_UNSUPPORTED and "kv_layout" in pa.last_error()
     n = pa.workspace_size(**args, dtype=w.dtype, num_sms=148)
     assert n == plan_ref.decode_header(_ref(w, num_sms=148))["total_bytes"]
 
