@@ -44,7 +44,7 @@ DEFAULT_WORKSPACE_BYTES = 128 * 1024 * 1024  # the timing script's workspace siz
 EXPORTED = ("pagedattn_plan", "pagedattn_workspace_size", "pagedattn_run", "pagedattn_run_stages",
             "pagedattn_plan_destroy", "pagedattn_last_error", "pagedattn_device_status",
             "pagedattn_debug_plan_dump", "pagedattn_debug_gather", "pagedattn_version",
-            "pagedattn_run_decode_noalloc")
+            "pagedattn_run_decode_noalloc", "pagedattn_plan_cascade", "pagedattn_workspace_size_cascade")
 
 
 class PagedAttnError(RuntimeError):
@@ -65,6 +65,25 @@ _lib = None
 _lock = threading.Lock()
 
 
+class PrefixGroups(ctypes.Structure):
+    """pagedattn_prefix_groups: requests [group_indptr[g], group_indptr[g+1])
+    share the full prefix pages prefix_page_indices[prefix_page_indptr[g] ..
+    prefix_page_indptr[g+1]) ahead of their own pages."""
+    _fields_ = [("group_indptr", ctypes.POINTER(ctypes.c_int32)),
+                ("prefix_page_indptr", ctypes.POINTER(ctypes.c_int32)),
+                ("prefix_page_indices", ctypes.POINTER(ctypes.c_int32)),
+                ("num_groups", ctypes.c_int32)]
+
+
+def _prefix_groups(prefix_groups):
+    """(group_indptr, prefix_page_indptr, prefix_page_indices) -> (struct, arrays kept alive)."""
+    arrs = [_i32(x) for x in prefix_groups]
+    g = PrefixGroups()
+    g.group_indptr, g.prefix_page_indptr, g.prefix_page_indices = (_ptr(a) for a in arrs)
+    g.num_groups = len(arrs[0]) - 1
+    return g, arrs
+
+
 def load() -> ctypes.CDLL:
     """Load the shared library (built by ``attention_paged_kv_gb300.build``)."""
     global _lib
@@ -82,6 +101,11 @@ def load() -> ctypes.CDLL:
         lib.pagedattn_plan.restype = ctypes.c_int
         lib.pagedattn_workspace_size.argtypes = plan_args + [ctypes.POINTER(Options), ctypes.POINTER(ctypes.c_size_t)]
         lib.pagedattn_workspace_size.restype = ctypes.c_int
+        pg = [ctypes.POINTER(PrefixGroups)]
+        lib.pagedattn_plan_cascade.argtypes = pg + lib.pagedattn_plan.argtypes
+        lib.pagedattn_plan_cascade.restype = ctypes.c_int
+        lib.pagedattn_workspace_size_cascade.argtypes = pg + lib.pagedattn_workspace_size.argtypes
+        lib.pagedattn_workspace_size_cascade.restype = ctypes.c_int
         lib.pagedattn_run.argtypes = [ctypes.c_void_p] * 4 + [ctypes.c_void_p, ctypes.c_void_p]
         lib.pagedattn_run.restype = ctypes.c_int
         lib.pagedattn_run_stages.argtypes = [ctypes.c_void_p] * 6 + [ctypes.c_uint32]
@@ -170,15 +194,17 @@ def _stream_handle(stream) -> int:
 
 
 def workspace_size(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_heads, num_kv_heads,
-                   head_dim, page_size, num_pages, dtype, causal=True, **opts) -> int:
+                   head_dim, page_size, num_pages, dtype, causal=True, prefix_groups=None, **opts) -> int:
     lib = load()
     a = [_i32(x) for x in (qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len)]
     n = ctypes.c_size_t(0)
     o = _options(**opts)
-    check(lib.pagedattn_workspace_size(_ptr(a[0]), _ptr(a[1]), _ptr(a[2]), _ptr(a[3]), len(a[0]) - 1,
-                                       int(num_qo_heads), int(num_kv_heads), int(head_dim), int(page_size),
-                                       int(num_pages), dtype_code(dtype), int(bool(causal)), ctypes.byref(o),
-                                       ctypes.byref(n)))
+    g, _keep = _prefix_groups(prefix_groups) if prefix_groups is not None else (None, None)
+    check(lib.pagedattn_workspace_size_cascade(ctypes.byref(g) if g is not None else None,
+                                               _ptr(a[0]), _ptr(a[1]), _ptr(a[2]), _ptr(a[3]), len(a[0]) - 1,
+                                               int(num_qo_heads), int(num_kv_heads), int(head_dim), int(page_size),
+                                               int(num_pages), dtype_code(dtype), int(bool(causal)), ctypes.byref(o),
+                                               ctypes.byref(n)))
     return int(n.value)
 
 
@@ -193,7 +219,7 @@ class Plan:
 
     def __init__(self, qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_heads, num_kv_heads,
                  head_dim, page_size, num_pages, dtype, causal=True, workspace=None, stream=None,
-                 host_only=False, **opts):
+                 host_only=False, prefix_groups=None, **opts):
         self._lib = load()
         self._h = ctypes.c_void_p(0)
         self.num_qo_heads, self.num_kv_heads = int(num_qo_heads), int(num_kv_heads)
@@ -213,17 +239,19 @@ class Plan:
             import torch
             if workspace is None:
                 need = workspace_size(*arrs, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, dtype,
-                                      causal, **opts)
+                                      causal, prefix_groups=prefix_groups, **opts)
                 workspace = torch.empty(max(need, DEFAULT_WORKSPACE_BYTES), dtype=torch.uint8, device="cuda")
             self.workspace = workspace
             ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
             st = _stream_handle(stream)
         else:
             self.workspace = None
-        check(self._lib.pagedattn_plan(_ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), _ptr(arrs[3]),
-                                       self.batch_size, self.num_qo_heads, self.num_kv_heads, self.head_dim,
-                                       self.page_size, self.num_pages, self.dtype_code, int(self.causal),
-                                       ws_ptr, ws_bytes, ctypes.byref(o), st, ctypes.byref(self._h)))
+        g, _keep = _prefix_groups(prefix_groups) if prefix_groups is not None else (None, None)
+        check(self._lib.pagedattn_plan_cascade(ctypes.byref(g) if g is not None else None,
+                                               _ptr(arrs[0]), _ptr(arrs[1]), _ptr(arrs[2]), _ptr(arrs[3]),
+                                               self.batch_size, self.num_qo_heads, self.num_kv_heads, self.head_dim,
+                                               self.page_size, self.num_pages, self.dtype_code, int(self.causal),
+                                               ws_ptr, ws_bytes, ctypes.byref(o), st, ctypes.byref(self._h)))
 
     # -- forward
     def run(self, q, kv_cache, out=None, lse=None, stream=None, return_lse=True,

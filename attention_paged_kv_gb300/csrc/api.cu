@@ -107,6 +107,10 @@ pagedattn_status fill_inputs(pa::PlanInputs* in, const int32_t* qo_indptr, const
                              int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
                              int32_t num_pages, pagedattn_dtype dtype, int32_t causal,
                              const pagedattn_options* opts) {
+  in->group_indptr = nullptr;
+  in->prefix_page_indptr = nullptr;
+  in->prefix_page_indices = nullptr;
+  in->n_groups = 0;
   in->qo_indptr = qo_indptr;
   in->kv_page_indptr = kv_page_indptr;
   in->kv_page_indices = kv_page_indices;
@@ -199,12 +203,29 @@ pagedattn_status pagedattn_workspace_size(const int32_t* qo_indptr, const int32_
                                           int32_t head_dim, int32_t page_size, int32_t num_pages,
                                           pagedattn_dtype dtype, int32_t causal, const pagedattn_options* opts,
                                           size_t* bytes) {
+  return pagedattn_workspace_size_cascade(nullptr, qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len,
+                                          batch_size, num_qo_heads, num_kv_heads, head_dim, page_size, num_pages,
+                                          dtype, causal, opts, bytes);
+}
+
+pagedattn_status pagedattn_workspace_size_cascade(const pagedattn_prefix_groups* groups, const int32_t* qo_indptr,
+                                                  const int32_t* kv_page_indptr, const int32_t* kv_page_indices,
+                                                  const int32_t* kv_last_page_len, int32_t batch_size,
+                                                  int32_t num_qo_heads, int32_t num_kv_heads, int32_t head_dim,
+                                                  int32_t page_size, int32_t num_pages, pagedattn_dtype dtype,
+                                                  int32_t causal, const pagedattn_options* opts, size_t* bytes) {
   g_last_error.clear();
   if (!bytes) return set_err(PA_ERR_INVALID_ARG, "bytes is NULL");
   pa::PlanInputs in;
   pagedattn_status s = fill_inputs(&in, qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, batch_size,
                                    num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, dtype, causal, opts);
   if (s != PA_OK) return s;
+  if (groups) {
+    in.group_indptr = groups->group_indptr;
+    in.prefix_page_indptr = groups->prefix_page_indptr;
+    in.prefix_page_indices = groups->prefix_page_indices;
+    in.n_groups = groups->num_groups;
+  }
   pa::HostPlan hp;
   std::string err;
   s = pa::build_plan(in, &hp, &err);
@@ -219,6 +240,18 @@ pagedattn_status pagedattn_plan(const int32_t* qo_indptr, const int32_t* kv_page
                                 int32_t num_pages, pagedattn_dtype dtype, int32_t causal, void* workspace,
                                 size_t workspace_bytes, const pagedattn_options* opts, pagedattn_stream_t stream,
                                 pagedattn_plan_t* out_plan) {
+  return pagedattn_plan_cascade(nullptr, qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, batch_size,
+                                num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, dtype, causal, workspace,
+                                workspace_bytes, opts, stream, out_plan);
+}
+
+pagedattn_status pagedattn_plan_cascade(const pagedattn_prefix_groups* groups, const int32_t* qo_indptr,
+                                        const int32_t* kv_page_indptr, const int32_t* kv_page_indices,
+                                        const int32_t* kv_last_page_len, int32_t batch_size, int32_t num_qo_heads,
+                                        int32_t num_kv_heads, int32_t head_dim, int32_t page_size,
+                                        int32_t num_pages, pagedattn_dtype dtype, int32_t causal, void* workspace,
+                                        size_t workspace_bytes, const pagedattn_options* opts,
+                                        pagedattn_stream_t stream, pagedattn_plan_t* out_plan) {
   g_last_error.clear();
   if (!out_plan) return set_err(PA_ERR_INVALID_ARG, "out_plan is NULL");
   *out_plan = nullptr;
@@ -226,6 +259,12 @@ pagedattn_status pagedattn_plan(const int32_t* qo_indptr, const int32_t* kv_page
   pagedattn_status s = fill_inputs(&in, qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, batch_size,
                                    num_qo_heads, num_kv_heads, head_dim, page_size, num_pages, dtype, causal, opts);
   if (s != PA_OK) return s;
+  if (groups) {
+    in.group_indptr = groups->group_indptr;
+    in.prefix_page_indptr = groups->prefix_page_indptr;
+    in.prefix_page_indices = groups->prefix_page_indices;
+    in.n_groups = groups->num_groups;
+  }
   pagedattn_plan_s* plan = new pagedattn_plan_s();
   std::string err;
   s = pa::build_plan(in, &plan->hp, &err);

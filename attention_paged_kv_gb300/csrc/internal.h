@@ -34,6 +34,11 @@ struct PlanInputs {
   const int32_t* kv_last_page_len;
   int32_t B, Hq, Hkv, D, ps, num_pages, dtype, causal;
   int32_t num_sms, force_prefill, decode_chunk_pages, prefill_chunk_tiles, decode_cuda_cores, kv_layout;
+  // shared-prefix cascade (n_groups == 0: a plain plan)
+  const int32_t* group_indptr;
+  const int32_t* prefix_page_indptr;
+  const int32_t* prefix_page_indices;
+  int32_t n_groups;
 };
 
 // Validate and partition; on failure returns the status and fills `err`.

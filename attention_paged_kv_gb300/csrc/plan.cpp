@@ -45,6 +45,23 @@
 //     prefill items by decreasing key count; ties in emission order.  The
 //     in-order block dispatch starts the longest items first, and each row
 //     class is one launch over consecutive items.
+//  7. Shared-prefix cascade (pagedattn_plan_cascade; the vLLM issue
+//     "Question about efficient memory sharing (prefix sharing)" asks to
+//     share the computation over a common prompt, not only its memory):
+//     the requests of group g, consecutive in the batch, share the full
+//     pages prefix_g ahead of their own pages, and every query row sits
+//     after that prefix.  The prefix attention of all the group's query
+//     tokens (consecutive in q) is one virtual request, index B + g, with
+//     no causal mask (its request entry has qo_len 0), planned as prefill
+//     items; each real request keeps only its own pages and mask.  Both
+//     levels always write partial rows, in one block per (group, kv head):
+//     S_g split slots (the prefix's splits first, then room for the most
+//     splits any of the group's requests has) of T_g * G rows, token-major,
+//     so that every (token, kv head) has its splits at one stride and the
+//     merge kernel combines them.  Emission order: everything of the plain
+//     requests as above, then group by group its requests' small-query
+//     items, its prefix items, its requests' prefill items, its merge
+//     entries (kv head, then token).
 #include <algorithm>
 #include <cstring>
 #include <string>
@@ -121,6 +138,40 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   }
   const int32_t T = B > 0 ? in.qo_indptr[B] : 0;
 
+  // -- rule 7: shared-prefix groups (none for a plain plan)
+  const int32_t NG = in.n_groups;
+  struct Grp { int32_t r0, r1, T, np, p0; };  // requests, query tokens, prefix pages, their offset
+  std::vector<Grp> grp(NG > 0 ? NG : 0);
+  std::vector<int32_t> grp_of(B, -1), tok_off(B, 0);
+  int64_t nnz_pre = 0;
+  if (NG < 0) return fail(err, PA_ERR_INVALID_ARG, "num_groups < 0");
+  if (NG > 0) {
+    if (!in.group_indptr || !in.prefix_page_indptr) return fail(err, PA_ERR_INVALID_ARG, "null group array");
+    if (in.group_indptr[0] != 0 || in.group_indptr[NG] != B || in.prefix_page_indptr[0] != 0)
+      return fail(err, PA_ERR_INVALID_ARG, "group_indptr must run from 0 to batch_size, prefix_page_indptr from 0");
+    nnz_pre = in.prefix_page_indptr[NG];
+    if (nnz_pre > 0 && !in.prefix_page_indices) return fail(err, PA_ERR_INVALID_ARG, "null prefix_page_indices");
+    for (int g = 0; g < NG; ++g) {
+      const int32_t r0 = in.group_indptr[g], r1 = in.group_indptr[g + 1];
+      const int32_t np = in.prefix_page_indptr[g + 1] - in.prefix_page_indptr[g];
+      if (r1 < r0 || np < 0) return fail(err, PA_ERR_INVALID_ARG, "group indptr arrays must be nondecreasing");
+      if (int64_t(np) * ps > INT32_MAX) return fail(err, PA_ERR_UNSUPPORTED, "prefix exceeds int32 keys");
+      grp[g] = {r0, r1, in.qo_indptr[r1] - in.qo_indptr[r0], np, int32_t(nnz + in.prefix_page_indptr[g])};
+      if (np > 0)
+        for (int b = r0; b < r1; ++b) {
+          grp_of[b] = g;
+          tok_off[b] = in.qo_indptr[b] - in.qo_indptr[r0];
+        }
+    }
+    for (int64_t i = 0; i < nnz_pre; ++i) {
+      const int32_t p = in.prefix_page_indices[i];
+      if (p < 0 || p >= in.num_pages)
+        return fail(err, PA_ERR_INVALID_ARG,
+                    "prefix_page_indices[" + std::to_string(i) + "]=" + std::to_string(p) + " out of range");
+    }
+  }
+  const int64_t nnz_all = nnz + nnz_pre;
+
   const bool dec_group = (G == 1 || G == 2 || G == 4 || G == 8 || G == 16);
   std::vector<char> is_dec(B, 0);
   bool multi_tok = false;
@@ -162,7 +213,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   std::vector<DecTmp> dec;
   std::vector<MergeEntry> merges;
   for (int b = 0; b < B; ++b) {
-    if (!is_dec[b]) continue;
+    if (!is_dec[b] || grp_of[b] >= 0) continue;
     const int64_t ns = cdiv(req[b].np, chunk);
     const int64_t R = int64_t(req[b].qo) * G;
     const int64_t qs = in.qo_indptr[b];
@@ -185,17 +236,30 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   // -- rule 4: prefill items
   const int32_t tq = kItemRows / G;
   struct Tile { int32_t b, t0, n; int64_t e; };
-  std::vector<Tile> tiles;
-  for (int b = 0; b < B; ++b) {
-    if (is_dec[b] || req[b].qo == 0) continue;
+  auto tiles_of = [&](int b, std::vector<Tile>& out) {
     for (int32_t t0 = 0; t0 < req[b].qo; t0 += tq) {
       const int32_t n = std::min(tq, req[b].qo - t0);
       const int64_t e = in.causal ? int64_t(req[b].kv) - req[b].qo + t0 + n : req[b].kv;
-      tiles.push_back({b, t0, n, e});
+      out.push_back({b, t0, n, e});
     }
+  };
+  std::vector<Tile> tiles;
+  for (int b = 0; b < B; ++b)
+    if (!is_dec[b] && req[b].qo > 0 && grp_of[b] < 0) tiles_of(b, tiles);
+  // cascade groups: the prefix tiles of virtual request B + g (every key
+  // visible), then the group's prefill requests
+  std::vector<std::vector<Tile>> gtiles(grp.size());
+  for (size_t g = 0; g < grp.size(); ++g) {
+    if (grp[g].np == 0 || grp[g].T == 0) continue;
+    for (int32_t t0 = 0; t0 < grp[g].T; t0 += tq)
+      gtiles[g].push_back({int32_t(B + g), t0, std::min(tq, grp[g].T - t0), int64_t(grp[g].np) * ps});
+    for (int b = grp[g].r0; b < grp[g].r1; ++b)
+      if (!is_dec[b] && req[b].qo > 0) tiles_of(b, gtiles[g]);
   }
   int64_t W = 0;
   for (auto& t : tiles) W += cdiv(t.e, kKvTile);
+  for (auto& gt : gtiles)
+    for (auto& t : gt) W += cdiv(t.e, kKvTile);
   W *= Hkv;
   const int64_t ctiles = in.prefill_chunk_tiles > 0 ? in.prefill_chunk_tiles
                                                     : std::max<int64_t>(8, cdiv(W, int64_t(2) * in.num_sms));
@@ -220,6 +284,59 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
       }
     }
   }
+
+  // -- rule 7: cascade blocks, items and merges, group by group
+  for (size_t g = 0; g < grp.size(); ++g) {
+    const Grp& gr = grp[g];
+    if (gr.np == 0 || gr.T == 0) continue;
+    const int64_t nsp = cdiv(cdiv(int64_t(gr.np) * ps, kKvTile), ctiles);  // prefix splits
+    auto tile_splits = [&](const Tile& t) { return cdiv(cdiv(t.e, kKvTile), ctiles); };
+    int64_t nsmax = 1;
+    for (int b = gr.r0; b < gr.r1; ++b)
+      if (is_dec[b]) nsmax = std::max(nsmax, cdiv(req[b].np, chunk));
+    for (const Tile& t : gtiles[g])
+      if (t.b < B) nsmax = std::max(nsmax, tile_splits(t));
+    const int64_t S = nsp + nsmax, TG = int64_t(gr.T) * G;
+    const int64_t base = part;
+    part += int64_t(Hkv) * S * TG;
+    auto row = [&](int h, int64_t s, int64_t tok) { return base + (h * S + s) * TG + tok * G; };
+    // the group's small-query requests
+    for (int b = gr.r0; b < gr.r1; ++b) {
+      if (!is_dec[b]) continue;
+      const int64_t ns = cdiv(req[b].np, chunk);
+      for (int h = 0; h < Hkv; ++h)
+        for (int64_t s2 = 0; s2 < ns; ++s2) {
+          const int64_t t0 = (s2 * req[b].np / ns) * ps;
+          const int64_t t1 = std::min<int64_t>(((s2 + 1) * req[b].np / ns) * ps, req[b].kv);
+          dec.push_back({b, h, int32_t(t0), int32_t(t1), int32_t(row(h, nsp + s2, tok_off[b])),
+                         row_class(int64_t(req[b].qo) * G)});
+        }
+    }
+    // the prefix tiles (all tokens of the group), then its prefill requests
+    for (const Tile& t : gtiles[g]) {
+      const int64_t ns = tile_splits(t);
+      const bool prefix = t.b >= B;
+      for (int h = 0; h < Hkv; ++h)
+        for (int64_t s2 = 0; s2 < ns; ++s2) {
+          const int64_t k0 = s2 * ctiles * kKvTile;
+          const int64_t k1 = std::min<int64_t>((s2 + 1) * ctiles * kKvTile, t.e);
+          const int64_t prow = prefix ? row(h, s2, t.t0) : row(h, nsp + s2, tok_off[t.b] + t.t0);
+          pre.push_back({t.b, h, t.t0, t.n, int32_t(k0), int32_t(k1), int32_t(prow)});
+        }
+    }
+    // one merge entry per (kv head, token): the prefix splits then the token's own
+    for (int h = 0; h < Hkv; ++h)
+      for (int b = gr.r0; b < gr.r1; ++b)
+        for (int32_t i = 0; i < req[b].qo; ++i) {
+          const int64_t own = is_dec[b] ? cdiv(req[b].np, chunk)
+                                        : tile_splits(Tile{b, (i / tq) * tq, 0,
+                                                           in.causal ? int64_t(req[b].kv) - req[b].qo +
+                                                                           std::min((i / tq + 1) * tq, req[b].qo)
+                                                                     : int64_t(req[b].kv)});
+          merges.push_back({int32_t((int64_t(in.qo_indptr[b]) + i) * Hq + h * G),
+                            int32_t(row(h, 0, tok_off[b] + i)), int32_t(nsp + own), int32_t(TG)});
+        }
+  }
   if (part > INT32_MAX / 256) return fail(err, PA_ERR_UNSUPPORTED, "too many partial rows");
 
   // -- rule 6: longest first, stable
@@ -234,8 +351,8 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
 
   // -- layout
   const int64_t off_pages = HDR_WORDS * 4;
-  const int64_t off_req = align256(off_pages + 4 * nnz);
-  const int64_t off_dec = align256(off_req + 16 * int64_t(B));
+  const int64_t off_req = align256(off_pages + 4 * nnz_all);
+  const int64_t off_dec = align256(off_req + 16 * int64_t(B + NG));
   const int64_t off_pre = align256(off_dec + 32 * int64_t(dec.size()));
   const int64_t off_merge = align256(off_pre + 32 * int64_t(pre.size()));
   const int64_t blob_bytes = align256(off_merge + 16 * int64_t(merges.size()));
@@ -247,7 +364,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   std::vector<int32_t>& blob = hp->blob;
   blob.assign(size_t(blob_bytes / 4), 0);
   const int32_t hdr[] = {kMagic, kVersion, B, Hq, Hkv, D, ps, in.num_pages, in.dtype, in.causal ? 1 : 0,
-                         T, int32_t(nnz), int32_t(dec.size()), int32_t(pre.size()), int32_t(merges.size()),
+                         T, int32_t(nnz_all), int32_t(dec.size()), int32_t(pre.size()), int32_t(merges.size()),
                          int32_t(part), int32_t(chunk), int32_t(ctiles), in.num_sms, G,
                          int32_t(off_pages), int32_t(off_req), int32_t(off_dec), int32_t(off_pre),
                          int32_t(off_merge), int32_t(blob_bytes), int32_t(off_part_o),
@@ -255,13 +372,22 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   std::memcpy(blob.data(), hdr, sizeof(hdr));
   for (int c = 0; c < kDecClasses; ++c) blob[H_NDEC_CLASS0 + c] = n_class[c];
   blob[H_LAYOUT] = in.kv_layout;
+  blob[H_NGROUPS] = NG;
   if (nnz) std::memcpy(blob.data() + off_pages / 4, in.kv_page_indices, size_t(4 * nnz));
+  if (nnz_pre) std::memcpy(blob.data() + off_pages / 4 + nnz, in.prefix_page_indices, size_t(4 * nnz_pre));
   for (int b = 0; b < B; ++b) {
     int32_t* r = blob.data() + off_req / 4 + 4 * b;
     r[0] = in.qo_indptr[b];
     r[1] = req[b].qo;
     r[2] = req[b].kv;
     r[3] = req[b].p0;
+  }
+  for (size_t g = 0; g < grp.size(); ++g) {  // virtual prefix requests: qo_len 0, i.e. every key visible
+    int32_t* r = blob.data() + off_req / 4 + 4 * (B + g);
+    r[0] = in.qo_indptr[grp[g].r0];
+    r[1] = 0;
+    r[2] = grp[g].np * ps;
+    r[3] = grp[g].p0;
   }
   for (size_t j = 0; j < dec.size(); ++j) {
     int32_t* r = blob.data() + off_dec / 4 + 8 * j;
@@ -278,7 +404,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   }
 
   hp->B = B; hp->Hq = Hq; hp->Hkv = Hkv; hp->D = D; hp->ps = ps; hp->num_pages = in.num_pages;
-  hp->dtype = in.dtype; hp->causal = in.causal ? 1 : 0; hp->T = T; hp->nnz = int32_t(nnz);
+  hp->dtype = in.dtype; hp->causal = in.causal ? 1 : 0; hp->T = T; hp->nnz = int32_t(nnz_all);
   hp->n_dec = int32_t(dec.size()); hp->n_pre = int32_t(pre.size()); hp->n_merge = int32_t(merges.size());
   hp->n_part = int32_t(part); hp->G = G; hp->num_sms = in.num_sms;
   hp->dec_cores = dec_cores;

@@ -43,8 +43,11 @@ WORKLOADS = {
     "decode": lambda wl: wl.decode(),
     "ragged": lambda wl: wl.ragged(),
     "prefix": lambda wl: wl.prefix(),
+    "prefix_cascade": lambda wl: wl.prefix(),
     "specdec": lambda wl: wl.mixed(prefill_len=0, decode_qo=4),
 }
+# workloads planned as a shared-prefix cascade: (group_indptr, prefix pages per group)
+CASCADE = {"prefix_cascade": ([0, 64], [12])}
 METRIC = "paged-attn prefill TFLOP/s & decode KV GB/s on 1 GB300, % of roofline"
 UNIT = "% of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -335,10 +338,14 @@ def main():
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     popts = {"decode_chunk_pages": args.decode_chunk_pages, "prefill_chunk_tiles": args.prefill_chunk_tiles}
-    need = pa.workspace_size(**w.plan_args(), dtype=w.dtype, **popts)
+    pargs = w.plan_args()
+    if args.workload in CASCADE:
+        groups, pargs = workloads.split_prefix(w, *CASCADE[args.workload])
+        popts["prefix_groups"] = groups
+    need = pa.workspace_size(**pargs, dtype=w.dtype, **popts)
     ws = torch.empty(max(need, pa.DEFAULT_WORKSPACE_BYTES), dtype=torch.uint8, device=dev)
     t_plan0 = time.perf_counter()
-    plan = pa.Plan(**w.plan_args(), dtype=w.dtype, workspace=ws, **popts)
+    plan = pa.Plan(**pargs, dtype=w.dtype, workspace=ws, **popts)
     t_plan = time.perf_counter() - t_plan0
     hdr = plan.dump()[:32]
     n_dec, n_pre, n_merge = int(hdr[12]), int(hdr[13]), int(hdr[14])
@@ -441,7 +448,7 @@ def main():
     # end to end through the public API: plan + pinned H2D of q + run + D2H of out/lse
     e2e = None
     if not args.no_e2e:
-        e2e = measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, max(1, args.e2e_steps), world, dev, hdr, popts)
+        e2e = measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, max(1, args.e2e_steps), world, dev, hdr, popts, pargs)
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -478,17 +485,19 @@ WORKLOAD_DESC = {
               "page_size 16, bf16",
     "prefix": "prefix sharing: 64 requests appending 30 tokens to one 200-token prompt (12 shared pages); "
               "Hq 32 / Hkv 8, head_dim 128, page_size 16, bf16",
+    "prefix_cascade": "the prefix-sharing batch planned as a shared-prefix cascade (the 12 shared pages "
+                      "attended once for all 64 requests)",
     "specdec": "speculative decoding: 256 requests x 4 query tokens, kv_len U[512,8192]; Hq 64 / Hkv 8, "
                "head_dim 128, page_size 16, bf16",
 }
 
 
-def measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, E, world, dev, hdr, popts):
+def measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, E, world, dev, hdr, popts, pargs):
     import torch
     q_h = w.q.pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     lse_h = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
-    args_plan = w.plan_args()
+    args_plan = pargs  # the timed plan's arguments (a cascade's own page tables included)
 
     def e2e_step():
         p2 = pa.Plan(**args_plan, dtype=w.dtype, workspace=ws, **popts)

@@ -161,6 +161,58 @@ PAGEDATTN_API pagedattn_status pagedattn_workspace_size(const int32_t* qo_indptr
                                           const pagedattn_options* opts, size_t* bytes);
 
 /*
+ * Shared-prefix cascade (the vLLM issue "Question about efficient memory
+ * sharing (prefix sharing)": requests that start from one system prompt
+ * should share its attention work, not only its pages).
+ *
+ * The requests of group g -- consecutive in the batch: requests
+ * [group_indptr[g], group_indptr[g+1]) -- all begin with the same prefix
+ * of full pages prefix_page_indices[prefix_page_indptr[g] ..
+ * prefix_page_indptr[g+1]), followed by their own pages as described by
+ * kv_page_indptr / kv_page_indices / kv_last_page_len (which then count only
+ * the keys after the prefix).  Request b of the group attends to
+ * prefix_len_g + kv_len_b keys: exactly what pagedattn_plan computes for the
+ * flattened page table (prefix pages, then the request's own), with the
+ * bottom-right causal mask over the whole sequence.  Its query rows must lie
+ * after the prefix (qo_len_b <= kv_len_b, the usual check on the request's
+ * own keys), so each of them sees the whole prefix.
+ *
+ * The plan computes the prefix attention once for all query tokens of the
+ * group (they are consecutive in q) as one unmasked prefill, the rest per
+ * request, and merges the two with the split-KV merge; results agree with
+ * the flattened plan within the usual tolerance (sums in another order).
+ * A group with no prefix pages is planned like ordinary requests.
+ */
+typedef struct {
+  const int32_t* group_indptr;        /* host, [num_groups + 1], [0] == 0, nondecreasing,
+                                         [num_groups] == batch_size                       */
+  const int32_t* prefix_page_indptr;  /* host, [num_groups + 1], [0] == 0, nondecreasing    */
+  const int32_t* prefix_page_indices; /* host, the groups' full prefix pages, each in
+                                         [0, num_pages)                                    */
+  int32_t num_groups;                 /* >= 0; 0 plans like pagedattn_plan                 */
+} pagedattn_prefix_groups;
+
+/* pagedattn_plan with shared-prefix groups (NULL groups: pagedattn_plan). */
+PAGEDATTN_API pagedattn_status pagedattn_plan_cascade(const pagedattn_prefix_groups* groups,
+                                        const int32_t* qo_indptr, const int32_t* kv_page_indptr,
+                                        const int32_t* kv_page_indices, const int32_t* kv_last_page_len,
+                                        int32_t batch_size, int32_t num_qo_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t page_size, int32_t num_pages,
+                                        pagedattn_dtype dtype, int32_t causal, void* workspace,
+                                        size_t workspace_bytes, const pagedattn_options* opts,
+                                        pagedattn_stream_t stream, pagedattn_plan_t* out_plan);
+
+/* pagedattn_workspace_size for pagedattn_plan_cascade. */
+PAGEDATTN_API pagedattn_status pagedattn_workspace_size_cascade(const pagedattn_prefix_groups* groups,
+                                          const int32_t* qo_indptr, const int32_t* kv_page_indptr,
+                                          const int32_t* kv_page_indices,
+                                          const int32_t* kv_last_page_len, int32_t batch_size,
+                                          int32_t num_qo_heads, int32_t num_kv_heads,
+                                          int32_t head_dim, int32_t page_size, int32_t num_pages,
+                                          pagedattn_dtype dtype, int32_t causal,
+                                          const pagedattn_options* opts, size_t* bytes);
+
+/*
  * Attention for the planned batch (the script's forward(q, kv_cache)).
  *
  * q        device, dtype[T, Hq, D] contiguous, 16-byte aligned (T = qo_indptr[B]).

@@ -62,9 +62,10 @@ start of the workspace:
                 off_pages, off_req, off_dec, off_pre, off_merge, blob_bytes,
                 off_part_o, off_part_lse, total_bytes, dec_cuda_cores, 0, 0,
                 [32] status word, [33..36] decode items per row class,
-                [37] cache layout (0 NHD, 1 HND), 0...
+                [37] cache layout (0 NHD, 1 HND), [38] shared-prefix groups, 0...
     pages[nnz]       copy of kv_page_indices
-    req[B][4]        qo_start, qo_len, kv_len, page_start
+    req[B + groups][4]  qo_start, qo_len, kv_len, page_start (group g's prefix: entry B + g,
+                     qo_len 0, its query tokens' qo_start, the prefix pages after the requests')
     dec[n_dec][8]    req, kv_head, tok0, tok1, part_row(-1 = direct), 0, 0, 0
     pre[n_pre][8]    req, kv_head, q_tok0, q_ntok, kv_tok0, kv_tok1, part_row, 0
     merge[n][4]      out_row0, part_row0, nsplit, split_stride
@@ -76,7 +77,7 @@ import numpy as np
 from .attention import PlanError, request_lengths
 
 MAGIC = 0x50414731
-VERSION = 3
+VERSION = 4
 HDR_WORDS = 64
 STATUS_WORD = 32
 Q_ROWS = 128       # packed query rows per prefill MMA tile (G must divide it)
@@ -109,8 +110,10 @@ def _align(x, a=256):
 def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_heads,
           num_kv_heads, head_dim, page_size, num_pages, dtype=BF16, causal=True, num_sms=148,
           force_prefill=False, decode_chunk_pages=0, prefill_chunk_tiles=0, decode_cuda_cores=False,
-          kv_layout="NHD"):
-    """Return the metadata blob (np.int32) the planner must produce."""
+          kv_layout="NHD", prefix_groups=None):
+    """Return the metadata blob (np.int32) the planner must produce.
+    ``prefix_groups`` = (group_indptr, prefix_page_indptr, prefix_page_indices)
+    plans a shared-prefix cascade (rule 7)."""
     Hq, Hkv, D, ps = int(num_qo_heads), int(num_kv_heads), int(head_dim), int(page_size)
     if Hq < 1 or Hkv < 1 or Hq % Hkv:
         raise PlanError("num_qo_heads must be a positive multiple of num_kv_heads")
@@ -139,6 +142,26 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
             raise PlanError("query rows without keys")
     T = int(np.asarray(qo_indptr)[-1])
 
+    # -- rule 7: shared-prefix groups: requests r0..r1-1, T_g query tokens,
+    # prefix of np_g full pages stored after the requests' pages
+    groups, grp_of, tok_off, pindices = [], [-1] * B, [0] * B, np.zeros(0, np.int64)
+    if prefix_groups is not None:
+        gind, pind = (np.asarray(x, np.int64) for x in prefix_groups[:2])
+        pindices = np.asarray(prefix_groups[2], np.int64)[:int(pind[-1])]
+        if gind[0] != 0 or gind[-1] != B or pind[0] != 0:
+            raise PlanError("group_indptr must run from 0 to batch_size")
+        if len(pindices) and (pindices.min() < 0 or pindices.max() >= num_pages):
+            raise PlanError("prefix page id out of range")
+        for g in range(len(gind) - 1):
+            r0, r1 = int(gind[g]), int(gind[g + 1])
+            npp = int(pind[g + 1] - pind[g])
+            groups.append((r0, r1, int(qo_indptr[r1]) - int(qo_indptr[r0]), npp, nnz + int(pind[g])))
+            if npp > 0:
+                for b in range(r0, r1):
+                    grp_of[b] = g
+                    tok_off[b] = int(qo_indptr[b]) - int(qo_indptr[r0])
+    NG = len(groups)
+
     is_dec = []
     for (qo, kv, _, _) in lens:
         d = (qo >= 1 and G in DECODE_GROUPS and not force_prefill and qo * G <= DEC_MAX_ROWS
@@ -164,7 +187,7 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
     part = 0
     dec, merges = [], []
     for b, ((qo, kv, p0, npg), d) in enumerate(zip(lens, is_dec)):
-        if not d:
+        if not d or grp_of[b] >= 0:
             continue
         ns = _cdiv(npg, chunk)
         R = qo * G
@@ -179,19 +202,33 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
             for s in range(ns):
                 t0 = (s * npg // ns) * ps
                 t1 = min(((s + 1) * npg // ns) * ps, kv)
-                dec.append((b, h, t0, t1, base + s * R if ns > 1 else -1, cls))
+                dec.append((b, h, t0, t1, base + s * R if ns > 1 else -1, -1, 0, cls))
 
     # -- prefill items (rule 4)
     tq = ITEM_ROWS // G
+
+    def tiles_of(b):
+        qo, kv = lens[b][0], lens[b][1]
+        return [(b, t0, min(tq, qo - t0), (kv - qo + t0 + min(tq, qo - t0)) if causal else kv)
+                for t0 in range(0, qo, tq)]
+
     tiles = []  # (b, t0, n, e)
     for b, ((qo, kv, p0, npg), d) in enumerate(zip(lens, is_dec)):
-        if d or qo == 0:
+        if d or qo == 0 or grp_of[b] >= 0:
             continue
-        for t0 in range(0, qo, tq):
-            n = min(tq, qo - t0)
-            e = kv - qo + t0 + n if causal else kv
-            tiles.append((b, t0, n, e))
-    W = sum(_cdiv(e, KV_TILE) for (_, _, _, e) in tiles) * Hkv
+        tiles += tiles_of(b)
+    # cascade: the prefix tiles of virtual request B + g (every key visible),
+    # then the group's prefill requests
+    gtiles = []
+    for g, (r0, r1, Tg, npp, _) in enumerate(groups):
+        gt = []
+        if npp > 0 and Tg > 0:
+            gt = [(B + g, t0, min(tq, Tg - t0), npp * ps) for t0 in range(0, Tg, tq)]
+            for b in range(r0, r1):
+                if not is_dec[b] and lens[b][0] > 0:
+                    gt += tiles_of(b)
+        gtiles.append(gt)
+    W = sum(_cdiv(e, KV_TILE) for (_, _, _, e) in tiles + [t for gt in gtiles for t in gt]) * Hkv
     ctiles = prefill_chunk_tiles if prefill_chunk_tiles > 0 else max(PRE_MIN_CHUNK_TILES, _cdiv(W, PRE_ITEMS_PER_SM * num_sms))
     pre = []
     for (b, t0, n, e) in tiles:
@@ -209,15 +246,68 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
                 k1 = min((s + 1) * ctiles * KV_TILE, e)
                 pre.append((b, h, t0, n, k0, k1, base + s * n * G if ns > 1 else -1))
 
+    # -- rule 7: cascade blocks, items and merges, group by group
+    def tile_splits(e):
+        return _cdiv(_cdiv(e, KV_TILE), ctiles)
+
+    for g, (r0, r1, Tg, npp, _) in enumerate(groups):
+        if npp == 0 or Tg == 0:
+            continue
+        nsp = tile_splits(npp * ps)
+        nsmax = 1
+        for b in range(r0, r1):
+            if is_dec[b]:
+                nsmax = max(nsmax, _cdiv(lens[b][3], chunk))
+        for (b, t0, n, e) in gtiles[g]:
+            if b < B:
+                nsmax = max(nsmax, tile_splits(e))
+        S, TG = nsp + nsmax, Tg * G
+        base = part
+        part += Hkv * S * TG
+
+        def row(h, s, tok):
+            return base + (h * S + s) * TG + tok * G
+
+        for b in range(r0, r1):
+            if not is_dec[b]:
+                continue
+            qo, kv, p0, npg = lens[b]
+            ns = _cdiv(npg, chunk)
+            cls = next(c for c, rows in enumerate(DEC_CLASS_ROWS) if qo * G <= rows)
+            for h in range(Hkv):
+                for s in range(ns):
+                    t0 = (s * npg // ns) * ps
+                    t1 = min(((s + 1) * npg // ns) * ps, kv)
+                    dec.append((b, h, t0, t1, row(h, nsp + s, tok_off[b]), -1, 0, cls))
+        for (b, t0, n, e) in gtiles[g]:
+            ns = tile_splits(e)
+            for h in range(Hkv):
+                for s in range(ns):
+                    k0 = s * ctiles * KV_TILE
+                    k1 = min((s + 1) * ctiles * KV_TILE, e)
+                    prow = row(h, s, t0) if b >= B else row(h, nsp + s, tok_off[b] + t0)
+                    pre.append((b, h, t0, n, k0, k1, prow))
+        for h in range(Hkv):
+            for b in range(r0, r1):
+                qo, kv, p0, npg = lens[b]
+                for i in range(qo):
+                    if is_dec[b]:
+                        own = _cdiv(npg, chunk)
+                    else:
+                        t0 = (i // tq) * tq
+                        own = tile_splits((kv - qo + min(t0 + tq, qo)) if causal else kv)
+                    merges.append(((int(qo_indptr[b]) + i) * Hq + h * G, row(h, 0, tok_off[b] + i), nsp + own, TG))
+
     # -- longest first, stable (rule 6)
-    dec = sorted(dec, key=lambda it: (it[5], -(it[3] - it[2])))
-    n_class = [sum(1 for it in dec if it[5] == c) for c in range(len(DEC_CLASS_ROWS))]
+    dec = sorted(dec, key=lambda it: (it[7], -(it[3] - it[2])))
+    n_class = [sum(1 for it in dec if it[7] == c) for c in range(len(DEC_CLASS_ROWS))]
     pre = sorted(pre, key=lambda it: -(it[5] - it[4]))
 
     # -- layout
     off_pages = HDR_WORDS * 4
-    off_req = _align(off_pages + 4 * nnz)
-    off_dec = _align(off_req + 16 * B)
+    nnz_all = nnz + len(pindices)
+    off_req = _align(off_pages + 4 * nnz_all)
+    off_dec = _align(off_req + 16 * (B + NG))
     off_pre = _align(off_dec + 32 * len(dec))
     off_merge = _align(off_pre + 32 * len(pre))
     blob_bytes = _align(off_merge + 16 * len(merges))
@@ -228,19 +318,23 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
         raise Unsupported("metadata and partial states exceed 2 GiB")
 
     blob = np.zeros(blob_bytes // 4, np.int32)
-    hdr = [MAGIC, VERSION, B, Hq, Hkv, D, ps, num_pages, dtype, int(bool(causal)), T, nnz,
+    hdr = [MAGIC, VERSION, B, Hq, Hkv, D, ps, num_pages, dtype, int(bool(causal)), T, nnz_all,
            len(dec), len(pre), len(merges), part, chunk, ctiles, num_sms, G,
            off_pages, off_req, off_dec, off_pre, off_merge, blob_bytes, off_part_o,
            off_part_lse, total, dec_cores]
     blob[:len(hdr)] = hdr
     blob[33:33 + len(n_class)] = n_class
     blob[37] = {"NHD": 0, "HND": 1}[kv_layout] if isinstance(kv_layout, str) else int(kv_layout)
+    blob[38] = NG
     blob[off_pages // 4: off_pages // 4 + nnz] = indices
+    blob[off_pages // 4 + nnz: off_pages // 4 + nnz_all] = pindices
     req = np.array([(int(qo_indptr[b]), qo, kv, p0) for b, (qo, kv, p0, _) in enumerate(lens)],
                    np.int32).reshape(-1, 4)
     blob[off_req // 4: off_req // 4 + 4 * B] = req.reshape(-1)
+    for g, (r0, r1, Tg, npp, pstart) in enumerate(groups):  # virtual prefix requests, qo_len 0
+        blob[off_req // 4 + 4 * (B + g): off_req // 4 + 4 * (B + g) + 4] = (int(qo_indptr[r0]), 0, npp * ps, pstart)
     for j, it in enumerate(dec):
-        blob[off_dec // 4 + 8 * j: off_dec // 4 + 8 * j + 5] = it[:5]
+        blob[off_dec // 4 + 8 * j: off_dec // 4 + 8 * j + 5] = it[:5]  # words 5..7 stay 0
     for j, it in enumerate(pre):
         blob[off_pre // 4 + 8 * j: off_pre // 4 + 8 * j + 7] = it
     for j, it in enumerate(merges):
@@ -255,6 +349,7 @@ def decode_header(blob: np.ndarray) -> dict:
              "off_merge", "blob_bytes", "off_part_o", "off_part_lse", "total_bytes", "dec_cuda_cores"]
     h = {n: int(blob[i]) for i, n in enumerate(names)}
     h["dec_class_items"] = [int(x) for x in blob[33:33 + len(DEC_CLASS_ROWS)]]
+    h["kv_layout"], h["n_groups"] = int(blob[37]), int(blob[38])
     return h
 
 

@@ -344,3 +344,52 @@ def test_hnd_layout_equals_nhd_bitexact(name, opts):
     if name in ("tiny", "smallq"):
         ro, rl = A.attention(w)
         assert_close(o2, l2, ro, rl, w.dtype, what=f"HND {name}")
+
+
+def _cascade_run(w, groups, args, kv=None, **opts):
+    plan = pa.Plan(**args, dtype=w.dtype, prefix_groups=groups, **opts)
+    out, lse = plan.run(w.q.cuda(), (w.kv_cache if kv is None else kv).cuda())
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    h = plan_ref.decode_header(plan.dump())
+    return out.double().cpu().numpy(), lse.double().cpu().numpy(), h
+
+
+def _cascade_mixed():
+    w = workloads.make_custom("cas", [30, 1, 4, 200, 1, 8, 1], [300, 500, 600, 900, 70, 400, 200], 16, 2,
+                              128, 16, dtype=torch.bfloat16, seed=51, permute_pages=False)
+    ind, ptr = w.kv_page_indices.copy(), w.kv_page_indptr
+    for b in (1, 2):
+        ind[ptr[b]:ptr[b] + 10] = ind[ptr[0]:ptr[0] + 10]
+    ind[ptr[4]:ptr[4] + 4] = ind[ptr[3]:ptr[3] + 4]
+    w.kv_page_indices = ind
+    return w, [0, 3, 5, 7], [10, 4, 0]
+
+
+def test_cascade_prefix_workload():
+    """The prefix batch (64 requests appending 30 tokens to a 200-token
+    prompt whose first 12 pages are shared) planned as a cascade: the
+    shared 192 keys are attended once for all 1920 query tokens."""
+    w = workloads.prefix()
+    groups, args = workloads.split_prefix(w, [0, 64], [12])
+    out, lse, h = _cascade_run(w, groups, args)
+    assert h["n_groups"] == 1
+    ro, rl = A.attention(w)
+    assert_close(out, lse, ro, rl, w.dtype, what="cascade prefix")
+    o2, l2, _ = run(w)
+    assert np.allclose(out, o2, atol=1e-2, rtol=0) and np.allclose(lse, l2, atol=1e-3, rtol=0)
+
+
+@pytest.mark.parametrize("opts", [{}, {"prefill_chunk_tiles": 1, "decode_chunk_pages": 3},
+                                  {"decode_cuda_cores": True}, {"kv_layout": "HND"}])
+def test_cascade_mixed_groups(opts):
+    """Groups of prefill, decode and few-token requests behind 10- and
+    4-page prefixes, and a group without one, against the oracle on the
+    flattened page tables."""
+    w, gind, npre = _cascade_mixed()
+    groups, args = workloads.split_prefix(w, gind, npre)
+    kv = w.kv_cache.permute(0, 1, 3, 2, 4).contiguous() if opts.get("kv_layout") == "HND" else None
+    out, lse, h = _cascade_run(w, groups, args, kv=kv, **opts)
+    assert h["n_groups"] == 3
+    ro, rl = A.attention(w)
+    assert_close(out, lse, ro, rl, w.dtype, what=f"cascade {opts}")

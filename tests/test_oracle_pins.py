@@ -414,3 +414,71 @@ def test_plan_ref_decode_script_split():
     assert h["n_part_rows"] == 128 * 2 * 8 and h["n_pre"] == 0
     dec, _, _ = plan_ref.items(blob)
     assert sorted({(int(a), int(b)) for a, b in dec[:, 2:4]}) == [(0, 512), (512, 1024)]
+
+
+@pytest.mark.parametrize("kw", [{}, {"prefill_chunk_tiles": 1, "decode_chunk_pages": 2}])
+def test_plan_ref_cascade_covers_every_pair_once(kw):
+    """Shared-prefix cascade plans: every (query token, head, key) of the
+    flattened sequence (prefix pages, then the request's own) is covered by
+    exactly one item -- the group's prefix items for prefix keys, the
+    request's items for its own -- and every partial row an item writes is
+    read by exactly one merge entry of its token."""
+    w = workloads.make_custom("t", [3, 1, 20, 2, 1], [40, 70, 60, 300, 30], 8, 2, 64, 4, seed=9,
+                              permute_pages=False)
+    ind, ptr = w.kv_page_indices.copy(), w.kv_page_indptr
+    for b in (1, 2):                      # requests 0-2 share 5 pages, requests 3-4 share 2
+        ind[ptr[b]:ptr[b] + 5] = ind[ptr[0]:ptr[0] + 5]
+    ind[ptr[4]:ptr[4] + 2] = ind[ptr[3]:ptr[3] + 2]
+    w.kv_page_indices = ind
+    gind, npre = [0, 3, 5], [5, 2]
+    groups, args = workloads.split_prefix(w, gind, npre)
+    blob = plan_ref.build(**{k: v for k, v in args.items() if k != "causal"}, causal=w.causal,
+                          dtype=plan_ref.FP16, num_sms=3, prefix_groups=groups, **kw)
+    h = plan_ref.decode_header(blob)
+    dec, pre, mer = plan_ref.items(blob)
+    G, Hq, ps, B = h["G"], h["Hq"], w.page_size, w.batch_size
+    own = A.request_lengths(args["qo_indptr"], args["kv_page_indptr"], args["kv_last_page_len"], ps)
+    pre_len = {b: npre[g] * ps for g in range(2) for b in range(gind[g], gind[g + 1])}
+    qi = np.asarray(w.qo_indptr)
+    tok_req = {int(qi[b]) + i: (b, i) for b in range(B) for i in range(own[b][0])}
+    cover, writes = {}, {}
+
+    def add(tok, head, key):
+        k = (tok, head, key)
+        assert k not in cover
+        cover[k] = 1
+
+    for (b, hk, t0, t1, pr, *_r) in dec:
+        qo, kv = own[b][0], own[b][1]
+        for i in range(qo):
+            for g in range(G):
+                for t in range(t0, min(t1, kv - qo + i + 1)):
+                    add(int(qi[b]) + i, hk * G + g, pre_len[b] + t)
+                if pr >= 0:
+                    writes[pr + i * G + g] = (int(qi[b]) + i, hk * G + g)
+    for (b, hk, q0, n, k0, k1, pr, _) in pre:
+        for i in range(q0, q0 + n):
+            for g in range(G):
+                if b >= B:                       # a group's prefix: every prefix key visible
+                    r0 = gind[b - B]
+                    tok = int(qi[r0]) + i
+                    keys = range(k0, k1)
+                else:
+                    qo, kv = own[b][0], own[b][1]
+                    tok = int(qi[b]) + i
+                    keys = [pre_len[b] + t for t in range(k0, min(k1, kv - qo + i + 1))]
+                for key in keys:
+                    add(tok, hk * G + g, key)
+                if pr >= 0:
+                    writes[pr + (i - q0) * G + g] = (tok, hk * G + g)
+    want = sum((pre_len[b] + own[b][1] - own[b][0] + i + 1) * Hq for b in range(B) for i in range(own[b][0]))
+    assert len(cover) == want
+    read = {}
+    for (o0, p0, ns, st) in mer:
+        tok, hk = divmod(o0, Hq)
+        for s in range(ns):
+            for g in range(G):
+                r = p0 + s * st + g
+                assert r not in read
+                read[r] = (tok, hk + g)
+    assert all(read.get(r) == th for r, th in writes.items())   # every written row merged into its own token

@@ -268,3 +268,49 @@ def test_exp2_polynomial_constants():
     y = bits.astype(np.uint32).view(np.float32).astype(np.float64)
     rel = np.abs(y / np.exp2(x.astype(np.float64)) - 1.0)
     assert rel.max() < 7.5e-5
+
+
+def _cascade_cases():
+    """(name, workload, group_indptr, prefix pages per group)."""
+    pre = workloads.prefix()                                    # 64 requests share 12 full pages
+    mixed = workloads.make_custom("cas", [30, 1, 4, 200, 1, 8, 1], [300, 500, 600, 900, 70, 400, 200], 16, 2,
+                                  128, 16, dtype=torch.bfloat16, seed=51, permute_pages=False)
+    # give requests 0-2 a common 10-page prefix and requests 3-4 a common 4-page one (tables rewritten)
+    ind = mixed.kv_page_indices.copy()
+    ptr = mixed.kv_page_indptr
+    for b in (1, 2):
+        ind[ptr[b]:ptr[b] + 10] = ind[ptr[0]:ptr[0] + 10]
+    ind[ptr[4]:ptr[4] + 4] = ind[ptr[3]:ptr[3] + 4]
+    mixed.kv_page_indices = ind
+    return [("prefix", pre, [0, 64], [12]), ("mixed", mixed, [0, 3, 5, 7], [10, 4, 0])]
+
+
+@pytest.mark.parametrize("case", [0, 1])
+@pytest.mark.parametrize("kw", [{}, {"prefill_chunk_tiles": 1, "decode_chunk_pages": 3}, {"decode_cuda_cores": True}])
+def test_cascade_plan_bit_exact_vs_restated_rules(lib, case, kw):
+    name, w, gind, npre = _cascade_cases()[case]
+    groups, args = workloads.split_prefix(w, gind, npre)
+    dt = plan_ref.FP16 if w.dtype == torch.float16 else plan_ref.BF16
+    want = plan_ref.build(**args, dtype=dt, num_sms=148, prefix_groups=groups, **kw)
+    p = pa.Plan(**args, dtype=w.dtype, host_only=True, num_sms=148, prefix_groups=groups, **kw)
+    got = p.dump()
+    p.close()
+    assert got.shape == want.shape and np.array_equal(got, want)
+    h = plan_ref.decode_header(got)
+    assert h["n_groups"] == len(gind) - 1 and h["n_pre"] > 0
+    n = pa.workspace_size(**args, dtype=w.dtype, num_sms=148, prefix_groups=groups, **kw)
+    assert n == h["total_bytes"]
+
+
+def test_cascade_plan_errors(lib):
+    name, w, gind, npre = _cascade_cases()[1]
+    groups, args = workloads.split_prefix(w, gind, npre)
+    bad = (np.array([0, 3, 6], np.int32), groups[1][:3], groups[2])      # groups end before batch_size
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.Plan(**args, dtype=w.dtype, host_only=True, num_sms=148, prefix_groups=bad)
+    assert e.value.status == pa.PA_ERR_INVALID_ARG
+    badp = groups[2].copy()
+    badp[0] = w.num_pages
+    with pytest.raises(pa.PagedAttnError) as e:
+        pa.Plan(**args, dtype=w.dtype, host_only=True, num_sms=148, prefix_groups=(groups[0], groups[1], badp))
+    assert e.value.status == pa.PA_ERR_INVALID_ARG

@@ -310,6 +310,31 @@ def mixed(num_decode: int = 256, prefill_len: int = 8192, kv_lo: int = 512, kv_h
                     np.asarray(kv, np.int64))
 
 
+def split_prefix(w: Workload, group_indptr, prefix_pages):
+    """Re-express a batch whose requests in each group begin with the same
+    full pages as a shared-prefix cascade: returns (prefix_groups, plan
+    arguments for the requests' own pages).  prefix_pages[g] pages are taken
+    off the front of every page list of group g (they must be identical)."""
+    gind = np.asarray(group_indptr, np.int64)
+    own_lists, pre_ind, pre_ptr = [], [], [0]
+    for g in range(len(gind) - 1):
+        k = int(prefix_pages[g])
+        lists = [w.kv_page_indices[w.kv_page_indptr[b]:w.kv_page_indptr[b + 1]] for b in range(gind[g], gind[g + 1])]
+        if k:
+            head = lists[0][:k]
+            assert all(np.array_equal(l[:k], head) for l in lists), "group pages differ"
+            pre_ind += [int(x) for x in head]
+        pre_ptr.append(len(pre_ind))
+        own_lists += [l[k:] for l in lists]
+    own_ptr = np.zeros(len(own_lists) + 1, np.int32)
+    own_ptr[1:] = np.cumsum([len(l) for l in own_lists])
+    own_ind = np.concatenate(own_lists).astype(np.int32) if own_lists else np.zeros(0, np.int32)
+    args = w.plan_args()
+    args.update(kv_page_indptr=own_ptr, kv_page_indices=own_ind)
+    groups = (np.asarray(gind, np.int32), np.asarray(pre_ptr, np.int32), np.asarray(pre_ind, np.int32))
+    return groups, args
+
+
 def by_name(name: str, **kw) -> Workload:
     return {"tiny": tiny, "decode": decode, "ragged": ragged, "prefix": prefix, "mixed": mixed}[name](**kw)
 
