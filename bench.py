@@ -8,8 +8,8 @@ kernel (tcgen05), the decode kernel and the split merge on one stream.
 
 The metric is the step's fraction of its roofline, in percent:
 roofline_time = max(F / P_tc, Bytes / BW_hbm), F = 4 * D * Hq * (visible
-query/key pairs), Bytes = q + out + lse + the unique K/V slots read + page
-ids; P_tc and BW_hbm are the measured peaks of the GPU.  Per-kernel figures
+query/key pairs), Bytes = q + out + lse + the unique K/V slots read (a page
+shared by several page tables counts once) + page ids; P_tc and BW_hbm are the measured peaks of the GPU.  Per-kernel figures
 (prefill TFLOP/s against the bf16 peak, decode KV GB/s against HBM) ride in
 the same JSON line.
 
@@ -44,10 +44,12 @@ WORKLOADS = {
     "ragged": lambda wl: wl.ragged(),
     "prefix": lambda wl: wl.prefix(),
     "prefix_cascade": lambda wl: wl.prefix(),
+    "prefix_decode": lambda wl: wl.prefix_decode(),
+    "prefix_decode_cascade": lambda wl: wl.prefix_decode(),
     "specdec": lambda wl: wl.mixed(prefill_len=0, decode_qo=4),
 }
 # workloads planned as a shared-prefix cascade: (group_indptr, prefix pages per group)
-CASCADE = {"prefix_cascade": ([0, 64], [12])}
+CASCADE = {"prefix_cascade": ([0, 64], [12]), "prefix_decode_cascade": ([0, 64], [256])}
 METRIC = "paged-attn prefill TFLOP/s & decode KV GB/s on 1 GB300, % of roofline"
 UNIT = "% of roofline"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -64,6 +66,18 @@ def visible_pairs(qo_lens, kv_lens, causal=True) -> int:
         if qo:
             tot += qo * (kv - qo) + qo * (qo + 1) // 2 if causal else qo * kv
     return tot
+
+
+def unique_slots(w, reqs) -> int:
+    """Distinct physical (page, slot) pairs the requests' keys occupy: a page
+    that several page tables share (a common prompt) is read once."""
+    used = {}
+    for b in reqs:
+        pages = w.kv_page_indices[w.kv_page_indptr[b]:w.kv_page_indptr[b + 1]]
+        for j, pg in enumerate(pages):
+            n = int(w.kv_last_page_len[b]) if j == len(pages) - 1 else w.page_size
+            used[int(pg)] = max(used.get(int(pg), 0), n)
+    return sum(used.values())
 
 
 def accounting(w):
@@ -83,7 +97,7 @@ def accounting(w):
         T = int(qo[sel].sum())
         pairs = visible_pairs(qo[sel], kv[sel], w.causal)
         F = 4 * D * Hq * pairs
-        kv_bytes = 2 * Hkv * D * e * int(kv[sel].sum())          # every slot read once
+        kv_bytes = 2 * Hkv * D * e * unique_slots(w, np.nonzero(sel)[0])  # shared pages count once
         io_bytes = T * Hq * D * e * 2 + T * Hq * 4 + 4 * int(npg[sel].sum())
         res[part] = {"flops": F, "kv_bytes": kv_bytes, "bytes": kv_bytes + io_bytes, "rows": T}
     res["flops"] = res["prefill"]["flops"] + res["decode"]["flops"]
@@ -487,6 +501,9 @@ WORKLOAD_DESC = {
               "Hq 32 / Hkv 8, head_dim 128, page_size 16, bf16",
     "prefix_cascade": "the prefix-sharing batch planned as a shared-prefix cascade (the 12 shared pages "
                       "attended once for all 64 requests)",
+    "prefix_decode": "64 one-token decodes continuing one 4096-token prompt (256 shared pages) plus "
+                     "U[100,500] own tokens; Hq 32 / Hkv 8, head_dim 128, page_size 16, bf16",
+    "prefix_decode_cascade": "the same 64 decodes planned as a shared-prefix cascade",
     "specdec": "speculative decoding: 256 requests x 4 query tokens, kv_len U[512,8192]; Hq 64 / Hkv 8, "
                "head_dim 128, page_size 16, bf16",
 }

@@ -393,3 +393,15 @@ def test_cascade_mixed_groups(opts):
     assert h["n_groups"] == 3
     ro, rl = A.attention(w)
     assert_close(out, lse, ro, rl, w.dtype, what=f"cascade {opts}")
+
+
+@pytest.mark.parametrize("cuda_cores", [False, True])
+def test_cascade_shared_prefix_decode(cuda_cores):
+    """One-token decodes continuing one long shared prompt, as a cascade:
+    the prompt's attention is one prefill over all the decodes' query rows."""
+    w = workloads.prefix_decode(batch_size=24, prefix_len=1024, own_lo=30, own_hi=300)
+    groups, args = workloads.split_prefix(w, [0, 24], [64])
+    out, lse, h = _cascade_run(w, groups, args, decode_cuda_cores=cuda_cores)
+    assert h["n_groups"] == 1 and h["n_pre"] > 0 and h["n_dec"] > 0
+    ro, rl = A.attention(w)
+    assert_close(out, lse, ro, rl, w.dtype, what="cascade decode")

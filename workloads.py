@@ -335,6 +335,38 @@ def split_prefix(w: Workload, group_indptr, prefix_pages):
     return groups, args
 
 
+def prefix_decode(batch_size: int = 64, prefix_len: int = 4096, own_lo: int = 100, own_hi: int = 500,
+                  num_qo_heads: int = 32, num_kv_heads: int = 8) -> Workload:
+    """``batch_size`` one-token decodes that all continue one ``prefix_len``-
+    token prompt (whole pages, physically shared: the same page ids open
+    every page list) followed by U[own_lo, own_hi] tokens of their own;
+    head_dim 128, page_size 16, bf16."""
+    s = _SEEDS["prefix"] * 100 + 50
+    ps, D = 16, 128
+    assert prefix_len % ps == 0
+    own = randint_incl(own_lo, own_hi, batch_size, s + 1)
+    shared = prefix_len // ps
+    own_pages = [pages_for(int(k), ps) for k in own]
+    n = shared + sum(own_pages)
+    perm = randperm(n, s + 2)
+    lists, nxt = [], shared
+    for np_b in own_pages:
+        lists.append(np.concatenate([perm[:shared], perm[nxt:nxt + np_b]]))
+        nxt += np_b
+    kv = [prefix_len + int(k) for k in own]
+    qo = [1] * batch_size
+    qo_indptr = np.zeros(batch_size + 1, np.int32)
+    qo_indptr[1:] = np.cumsum(qo)
+    kv_page_indptr = np.zeros(batch_size + 1, np.int32)
+    kv_page_indptr[1:] = np.cumsum([len(l) for l in lists])
+    kv_page_indices = np.concatenate(lists).astype(np.int32)
+    kv_last = np.array([last_page_len(k, ps) for k in kv], np.int32)
+    q = randn((batch_size, num_qo_heads, D), torch.bfloat16, s + 3)
+    cache = randn((n, 2, ps, num_kv_heads, D), torch.bfloat16, s + 4, chunk_rows=512)
+    return Workload("prefix_decode", qo_indptr, kv_page_indptr, kv_page_indices, kv_last, num_qo_heads,
+                    num_kv_heads, D, ps, n, torch.bfloat16, True, q, cache, np.asarray(kv, np.int64))
+
+
 def by_name(name: str, **kw) -> Workload:
     return {"tiny": tiny, "decode": decode, "ragged": ragged, "prefix": prefix, "mixed": mixed}[name](**kw)
 
