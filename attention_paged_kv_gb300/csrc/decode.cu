@@ -707,32 +707,53 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
   asm volatile("bar.sync 2, 128;" ::: "memory");
   if (*abort_flag) return;
   const bool partial = it.part_row >= 0;
-  for (int idx = tid; idx < 16 * RGN * D; idx += 128) {
-    const int r = idx / D, d = idx % D;
-    if (r >= R) break;  // rows are visited in increasing order
+  // per row: the key subsets' weights exp2(m_k - M) / L once, and the lse
+  float* comb_w = comb_l + 4 * 16;  // [rows][KS]
+  for (int r = tid; r < R; r += 128) {
     const int rgr = r >> 4, rr = r & 15;
     float M = -INFINITY;
 #pragma unroll
     for (int k = 0; k < KS; ++k) M = fmaxf(M, comb_m[(rgr + k * RGN) * 16 + rr]);
     const float Mu = (M == -INFINITY) ? 0.f : M;
-    float L = 0.f, O = 0.f;
+    float wk[KS], L = 0.f;
 #pragma unroll
     for (int k = 0; k < KS; ++k) {
-      const int w = rgr + k * RGN;
-      const float wq = ex2f(comb_m[w * 16 + rr] - Mu);
-      L += wq * comb_l[w * 16 + rr];
-      O += wq * comb_o[(w * 16 + rr) * D + d];
+      wk[k] = ex2f(comb_m[(rgr + k * RGN) * 16 + rr] - Mu);
+      L += wk[k] * comb_l[(rgr + k * RGN) * 16 + rr];
     }
-    const float val = L > 0.f ? O / L : 0.f;
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+#pragma unroll
+    for (int k = 0; k < KS; ++k) comb_w[r * KS + k] = wk[k] * inv;
     const float lse = L > 0.f ? (Mu + __log2f(L)) * kLn2f : -INFINITY;
     if (!partial) {
-      const int64_t orow = int64_t(rq.qo_start + (r >> p.g_shift)) * p.Hq + int64_t(it.kv_head) * p.G +
-                           (r & (p.G - 1));
-      static_cast<T*>(p.out)[orow * D + d] = Elt<T>::from_f(val);
-      if (d == 0 && p.lse) p.lse[orow] = lse;
+      if (p.lse) p.lse[row_of(r)] = lse;
     } else {
-      p.part_o[(int64_t(it.part_row) + r) * D + d] = val;
-      if (d == 0) p.part_lse[it.part_row + r] = lse;
+      p.part_lse[it.part_row + r] = lse;
+    }
+  }
+  asm volatile("bar.sync 2, 128;" ::: "memory");
+  // O: four columns a thread at a time, a weighted sum over the key subsets
+  constexpr int C4 = D / 4;
+  for (int idx = tid; idx < R * C4; idx += 128) {
+    const int r = idx / C4, c = idx % C4;
+    const int rgr = r >> 4, rr = r & 15;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < KS; ++k) {
+      const float w = comb_w[r * KS + k];
+      const float4 v = *reinterpret_cast<const float4*>(&comb_o[((rgr + k * RGN) * 16 + rr) * D + 4 * c]);
+      acc.x = fmaf(w, v.x, acc.x);
+      acc.y = fmaf(w, v.y, acc.y);
+      acc.z = fmaf(w, v.z, acc.z);
+      acc.w = fmaf(w, v.w, acc.w);
+    }
+    if (!partial) {
+      uint2 pk;
+      pk.x = Elt<T>::from_f2(acc.x, acc.y);
+      pk.y = Elt<T>::from_f2(acc.z, acc.w);
+      *reinterpret_cast<uint2*>(static_cast<T*>(p.out) + row_of(r) * D + 4 * c) = pk;
+    } else {
+      *reinterpret_cast<float4*>(p.part_o + (int64_t(it.part_row) + r) * D + 4 * c) = acc;
     }
   }
 }
