@@ -559,8 +559,8 @@ def measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, E, world, dev, hdr, popts, p
 
     def piped_step(i):
         sl = slots[i % 2]
-        if sl["plan"] is not None:      # this slot's previous step must be fully back
-            sl["d2h"].synchronize()
+        if sl["plan"] is not None:      # at most two steps in flight: this slot's last run is done
+            sl["run"].synchronize()
             sl["plan"].close()
         plan = pa.Plan(**args_plan, dtype=w.dtype, workspace=sl["ws"], stream=cs, **popts)
         xs.wait_event(sl["run"])        # the slot's q is free once its last run is done
@@ -568,6 +568,7 @@ def measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, E, world, dev, hdr, popts, p
             sl["q"].copy_(q_h, non_blocking=True)
         sl["h2d"].record(xs)
         cs.wait_event(sl["h2d"])
+        cs.wait_event(sl["d2h"])        # the slot's out / lse have been read back
         plan.run(sl["q"], kv, out=sl["out"], lse=sl["lse"], stream=cs)
         sl["run"].record(cs)
         ys.wait_event(sl["run"])
