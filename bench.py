@@ -68,6 +68,15 @@ def visible_pairs(qo_lens, kv_lens, causal=True) -> int:
     return tot
 
 
+def max_over_ranks(values, device):
+    """Element-wise maximum of per-rank timings over the process group (each
+    rank runs its own replica of the batch; the slowest sets the step)."""
+    import torch
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return [float(x) for x in t.tolist()]
+
+
 def unique_slots(w, reqs) -> int:
     """Distinct physical (page, slot) pairs the requests' keys occupy: a page
     that several page tables share (a common prompt) is read once."""
@@ -425,9 +434,7 @@ def main():
         t_mrg = sum(e[2].elapsed_time(e[3]) for e in ev) / K if n_merge else 0.0
     assert plan.device_status() == 0, pa.last_error()
     if world > 1:
-        tt = torch.tensor([total_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(tt.item())
+        (total_ms,) = max_over_ranks([total_ms], dev)
     ms_per_step = total_ms / K
 
     long_run = total_ms >= 1000.0
@@ -590,9 +597,7 @@ def measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, E, world, dev, hdr, popts, p
         if sl["plan"] is not None:
             sl["plan"].close()
     if world > 1:
-        tt = torch.tensor([e2e_ms, serial_ms], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms, serial_ms = float(tt[0].item()), float(tt[1].item())
+        e2e_ms, serial_ms = max_over_ranks([e2e_ms, serial_ms], dev)
     h2d = q.numel() * q.element_size() + int(hdr[25])
     d2h = out.numel() * out.element_size() + lse.numel() * 4
     e2e = {"value": 100.0 * roof_t / (e2e_ms * 1e-3), "unit": UNIT, "ms_per_step": e2e_ms,
