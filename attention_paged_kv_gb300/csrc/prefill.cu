@@ -125,13 +125,11 @@ __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   }
 }
 
-__device__ __forceinline__ float max32(const uint32_t (&r)[32]) {
-  float m[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i)
-    m[i] = fmaxf(fmaxf(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1])),
-                 fmaxf(__uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3])));
-  return fmaxf(fmaxf(fmaxf(m[0], m[1]), fmaxf(m[2], m[3])), fmaxf(fmaxf(m[4], m[5]), fmaxf(m[6], m[7])));
+// Three-input maximum (one instruction on sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
 }
 
 template <typename T, int D>
@@ -405,10 +403,20 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         for (int i = 0; i < 128; ++i)
           if (i >= lim) s[i] = __float_as_uint(-INFINITY);
       }
-      float mx = fmaxf(fmaxf(max32(*reinterpret_cast<uint32_t(*)[32]>(s + 0)),
-                             max32(*reinterpret_cast<uint32_t(*)[32]>(s + 32))),
-                       fmaxf(max32(*reinterpret_cast<uint32_t(*)[32]>(s + 64)),
-                             max32(*reinterpret_cast<uint32_t(*)[32]>(s + 96))));
+      // row max as a tree of three-input maxima: 128 -> 43 -> 15 -> 5 -> 1
+      float m43[43];
+#pragma unroll
+      for (int u = 0; u < 42; ++u)
+        m43[u] = fmax3(__uint_as_float(s[3 * u]), __uint_as_float(s[3 * u + 1]), __uint_as_float(s[3 * u + 2]));
+      m43[42] = fmaxf(__uint_as_float(s[126]), __uint_as_float(s[127]));
+      float m15[15];
+#pragma unroll
+      for (int u = 0; u < 14; ++u) m15[u] = fmax3(m43[3 * u], m43[3 * u + 1], m43[3 * u + 2]);
+      m15[14] = m43[42];
+      float m5[5];
+#pragma unroll
+      for (int u = 0; u < 5; ++u) m5[u] = fmax3(m15[3 * u], m15[3 * u + 1], m15[3 * u + 2]);
+      float mx = fmax3(fmax3(m5[0], m5[1], m5[2]), m5[3], m5[4]);
       const float mx2 = mx * sl2;
       float alpha = 1.f;
       bool resc = false;
