@@ -80,35 +80,6 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// 2^x for a pair of x <= 0 on the FMA and integer pipes, to take part of the
-// softmax's exponentials off the multi-function unit (one row of S needs 128
-// of them; that unit does 4 a clock per SM sub-partition).  Cody-Waite range
-// reduction: x = r + f with r = round(x) (read off the mantissa of x + 1.5 *
-// 2^23) and f in [-1/2, 1/2]; 2^f from a cubic fitted to it on that interval
-// by iterated reweighted least squares (relative error below 7.5e-5, 2^-13.7;
-// exp2_poly_fit.py beside this file derives the coefficients); 2^r is added
-// to the exponent field.  x is clamped at -125 first so the exponent stays
-// normal: a masked key (x = -inf) yields about 2e-38 instead of 0.
-constexpr float kExp2C0 = 0.9999280571937561f, kExp2C1 = 0.6932609677314758f;
-constexpr float kExp2C2 = 0.2426111400127411f, kExp2C3 = 0.0551716685295105f;
-__device__ __forceinline__ float2 exp2_fma2(float2 x) {
-  constexpr float kRound = 12582912.0f;  // 1.5 * 2^23
-  x.x = fmaxf(x.x, -125.f);
-  x.y = fmaxf(x.y, -125.f);
-  const float2 t = __fadd2_rn(x, make_float2(kRound, kRound));
-  const float2 r = __fadd2_rn(t, make_float2(-kRound, -kRound));
-  const float2 f = __ffma2_rn(r, make_float2(-1.f, -1.f), x);
-  float2 q = __ffma2_rn(f, make_float2(kExp2C3, kExp2C3), make_float2(kExp2C2, kExp2C2));
-  q = __ffma2_rn(q, f, make_float2(kExp2C1, kExp2C1));
-  q = __ffma2_rn(q, f, make_float2(kExp2C0, kExp2C0));
-  return make_float2(__uint_as_float(__float_as_uint(q.x) + (__float_as_uint(t.x) << 23)),
-                     __uint_as_float(__float_as_uint(q.y) + (__float_as_uint(t.y) << 23)));
-}
-
-// Which pairs of each 32-column chunk take the polynomial: 6 of 16 (3/8 of
-// the exponentials), which balances the multi-function unit against issue.
-__device__ __forceinline__ constexpr bool poly_pair(int i) { return (i & 7) == 0 || (i & 7) == 3 || (i & 7) == 6; }
-
 // Bounded wait, made uniform across the warp (all lanes leave together).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
                                           int32_t* status) {
@@ -437,13 +408,13 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       }
 
       // p = exp2(s * scale_log2 - m), row sum, P (hi) into TMEM over S.  The
-      // first key tile of a sequence (P split into hi + lo) takes every
-      // exponential from the multi-function unit; the others send 3/8 of them
-      // through exp2_fma2.
+      // row sum runs in four independent chains (one long chain of dependent
+      // adds would set the pace).  The first key tile of a sequence is
+      // compiled apart: only there may P be split into hi + lo.
       const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
-      auto softmax_p = [&](auto poly_tag) -> float {
-        constexpr bool kPoly = decltype(poly_tag)::value;
-        float2 acc2 = make_float2(0.f, 0.f);
+      auto softmax_p = [&](auto first_tag) -> float {
+        constexpr bool kFirst = decltype(first_tag)::value;
+        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t ph[16];
@@ -455,23 +426,15 @@ __global__ void __launch_bounds__(kPreThreads, 1)
               const int i = 4 * u + v, k = 32 * c + 2 * i;
               const float2 t2 =
                   __ffma2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), sc2, nm2);
-              float a, b;
-              if (kPoly && poly_pair(i)) {
-                const float2 e = exp2_fma2(t2);
-                a = e.x;
-                b = e.y;
-              } else {
-                a = ex2(t2.x);
-                b = ex2(t2.y);
-              }
-              acc2 = __fadd2_rn(acc2, make_float2(a, b));
+              const float a = ex2(t2.x), b = ex2(t2.y);
+              acc[u] = __fadd2_rn(acc[u], make_float2(a, b));
               ph[i] = Elt<T>::from_f2(a, b);
-              if (!kPoly && lo_split) {
+              if (kFirst && lo_split) {
                 const float2 hi = Elt<T>::to_f2(ph[i]);
                 lw[v] = Elt<T>::from_f2(a - hi.x, b - hi.y);
               }
             }
-            if (!kPoly && lo_split) {
+            if (kFirst && lo_split) {
               // keys 32c + 8u .. +7 of row r -> K-major 128-byte-swizzled smem
               const int cc = (c & 1) * 4 + u;
               *reinterpret_cast<uint4*>(smem + plo_off(x) + (c >> 1) * C::BLK + r * 128 + ((cc ^ (r & 7)) * 16)) =
@@ -480,12 +443,12 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           }
           tmem_st16(s_col + c * 16, ph);
         }
-        return acc2.x + acc2.y;
+        const float2 sum = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        return sum.x + sum.y;
       };
-      const float rs = (j == 0) ? softmax_p(std::false_type{}) : softmax_p(std::true_type{});
+      const float rs = (j == 0) ? softmax_p(std::true_type{}) : softmax_p(std::false_type{});
       // S_x(j) done implies PV_x(j-1) done (the MMAs run in issue order); the
       // barrier makes O's contents visible before it is rescaled
-      // PV of the previous tile must be done before O is rescaled
       if (j >= 1) {
         ok = warp_wait(&o_done[x], (j - 1) & 1, abort_flag, p.status);
         if (!ok) break;

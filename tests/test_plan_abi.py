@@ -242,34 +242,6 @@ def test_plan_small_query_semantics(lib):
     assert hb["dec_cuda_cores"] == 0 and hb["n_pre"] == 0 and hb["dec_class_items"][0] == hb["n_dec"]
 
 
-def test_exp2_polynomial_constants():
-    """The cubic in prefill.cu's exp2_fma2: its float32 coefficients are the
-    fit that exp2_poly_fit.py derives, and the full evaluation (range
-    reduction by rounding, cubic on f in [-1/2, 1/2], exponent add) stays
-    within the stated relative error of 2^x on the range the softmax uses."""
-    import importlib.util
-    import re
-    csrc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "attention_paged_kv_gb300", "csrc")
-    src = open(os.path.join(csrc, "prefill.cu")).read()
-    got = [float(re.search(rf"kExp2C{i} = ([0-9.e+-]+)f", src).group(1)) for i in range(4)]
-    spec = importlib.util.spec_from_file_location("exp2_poly_fit", os.path.join(csrc, "exp2_poly_fit.py"))
-    fitmod = importlib.util.module_from_spec(spec)
-    spec.loader.exec_module(fitmod)
-    want = fitmod.fit()
-    assert np.allclose(np.float32(got), want, rtol=0, atol=2e-7)
-    c = np.float32(got)
-    x = np.concatenate([np.linspace(-125.0, 0.0, 400001), -np.logspace(-8, 0, 1000)]).astype(np.float32)
-    t = (x + np.float32(12582912.0)).astype(np.float32)
-    r = (t - np.float32(12582912.0)).astype(np.float32)
-    f = (x - r).astype(np.float32)
-    assert np.abs(f).max() <= 0.5
-    q = ((((c[3] * f + c[2]).astype(np.float32) * f + c[1]).astype(np.float32) * f) + c[0]).astype(np.float32)
-    bits = (q.view(np.uint32).astype(np.uint64) + (t.view(np.uint32).astype(np.uint64) << np.uint64(23))) & 0xFFFFFFFF
-    y = bits.astype(np.uint32).view(np.float32).astype(np.float64)
-    rel = np.abs(y / np.exp2(x.astype(np.float64)) - 1.0)
-    assert rel.max() < 7.5e-5
-
-
 def _cascade_cases():
     """(name, workload, group_indptr, prefix pages per group)."""
     pre = workloads.prefix()                                    # 64 requests share 12 full pages
