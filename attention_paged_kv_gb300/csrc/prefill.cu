@@ -408,13 +408,13 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       }
 
       // p = exp2(s * scale_log2 - m), row sum, P (hi) into TMEM over S.  The
-      // row sum runs in four independent chains (one long chain of dependent
-      // adds would set the pace).  The first key tile of a sequence is
+      // row sum runs in two independent chains (one long chain of dependent
+      // adds would set the pace; more chains cost registers).  The first key tile of a sequence is
       // compiled apart: only there may P be split into hi + lo.
       const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
       auto softmax_p = [&](auto first_tag) -> float {
         constexpr bool kFirst = decltype(first_tag)::value;
-        float2 acc[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+        float2 acc[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
 #pragma unroll
         for (int c = 0; c < 4; ++c) {
           uint32_t ph[16];
@@ -427,7 +427,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
               const float2 t2 =
                   __ffma2_rn(make_float2(__uint_as_float(s[k]), __uint_as_float(s[k + 1])), sc2, nm2);
               const float a = ex2(t2.x), b = ex2(t2.y);
-              acc[u] = __fadd2_rn(acc[u], make_float2(a, b));
+              acc[u & 1] = __fadd2_rn(acc[u & 1], make_float2(a, b));
               ph[i] = Elt<T>::from_f2(a, b);
               if (kFirst && lo_split) {
                 const float2 hi = Elt<T>::to_f2(ph[i]);
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
           }
           tmem_st16(s_col + c * 16, ph);
         }
-        const float2 sum = __fadd2_rn(__fadd2_rn(acc[0], acc[1]), __fadd2_rn(acc[2], acc[3]));
+        const float2 sum = __fadd2_rn(acc[0], acc[1]);
         return sum.x + sum.y;
       };
       const float rs = (j == 0) ? softmax_p(std::true_type{}) : softmax_p(std::false_type{});
