@@ -862,21 +862,25 @@ cudaError_t launch_decode_d(const RunArgs& a, const CUtensorMap* map, const KPar
       default: return cudaErrorInvalidValue;
     }
   }
-  int item0 = 0;
-  for (int c = 0; c < kDecClasses; ++c) {
-    const int n = hp.n_dec_class[c];
-    if (n == 0) continue;
-    cudaError_t e = cudaSuccess;
-    switch (c) {
-      case 0: e = launch_mma<T, D, 0>(a, m, kp, use_tma, item0, n); break;
-      case 1: e = launch_mma<T, D, 1>(a, m, kp, use_tma, item0, n); break;
-      case 2: e = launch_mma<T, D, 2>(a, m, kp, use_tma, item0, n); break;
-      default: e = launch_mma<T, D, 3>(a, m, kp, use_tma, item0, n); break;
+  if constexpr (D == 256) {
+    return cudaErrorInvalidValue;  // no warp-MMA kernel at head_dim 256
+  } else {
+    int item0 = 0;
+    for (int c = 0; c < kDecClasses; ++c) {
+      const int n = hp.n_dec_class[c];
+      if (n == 0) continue;
+      cudaError_t e = cudaSuccess;
+      switch (c) {
+        case 0: e = launch_mma<T, D, 0>(a, m, kp, use_tma, item0, n); break;
+        case 1: e = launch_mma<T, D, 1>(a, m, kp, use_tma, item0, n); break;
+        case 2: e = launch_mma<T, D, 2>(a, m, kp, use_tma, item0, n); break;
+        default: e = launch_mma<T, D, 3>(a, m, kp, use_tma, item0, n); break;
+      }
+      if (e != cudaSuccess) return e;
+      item0 += n;
     }
-    if (e != cudaSuccess) return e;
-    item0 += n;
+    return item0 == hp.n_dec ? cudaSuccess : cudaErrorInvalidValue;
   }
-  return item0 == hp.n_dec ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -890,6 +894,8 @@ cudaError_t launch_decode(const RunArgs& a, const CUtensorMap* map_rows) {
   const bool bf = a.hp->dtype == PA_BF16;
   if (a.hp->D == 128)
     return bf ? launch_decode_d<__nv_bfloat16, 128>(a, map_rows, kp) : launch_decode_d<__half, 128>(a, map_rows, kp);
+  if (a.hp->D == 256)
+    return bf ? launch_decode_d<__nv_bfloat16, 256>(a, map_rows, kp) : launch_decode_d<__half, 256>(a, map_rows, kp);
   return bf ? launch_decode_d<__nv_bfloat16, 64>(a, map_rows, kp) : launch_decode_d<__half, 64>(a, map_rows, kp);
 }
 
@@ -902,6 +908,9 @@ cudaError_t launch_merge(const RunArgs& a) {
   if (a.hp->D == 128) {
     if (bf) merge_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, a.stream>>>(kp, rows);
     else merge_kernel<__half, 128><<<blocks, 256, 0, a.stream>>>(kp, rows);
+  } else if (a.hp->D == 256) {
+    if (bf) merge_kernel<__nv_bfloat16, 256><<<blocks, 256, 0, a.stream>>>(kp, rows);
+    else merge_kernel<__half, 256><<<blocks, 256, 0, a.stream>>>(kp, rows);
   } else {
     if (bf) merge_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, a.stream>>>(kp, rows);
     else merge_kernel<__half, 64><<<blocks, 256, 0, a.stream>>>(kp, rows);

@@ -13,12 +13,14 @@
 //     (token, head) rows number at most 64 (one decoded token, or a few
 //     speculative ones) and, when qo_b > 1, that has more keys than one
 //     prefill key tile (kv_b > 128; a shorter one costs the prefill kernel
-//     a single key tile), unless force_prefill.  With decode_cuda_cores only
-//     qo_b == 1 at G <= 8 qualifies (the CUDA-core kernel's shapes).  Every
-//     other request with rows -> tensor-core prefill.  The decode items run
-//     on the CUDA-core kernel when decode_cuda_cores is set, or when G <= 2
-//     and every small-query request has qo_b == 1; else on the warp-MMA
-//     kernel.  Row class of an item: R_b <= 8, 16, 32 or 64.
+//     a single key tile), unless force_prefill.  With decode_cuda_cores, or
+//     at head_dim 256 (where the warp-MMA kernel's fragments would not fit
+//     in registers), only qo_b == 1 at G <= 8 qualifies (the CUDA-core
+//     kernel's shapes).  Every other request with rows -> tensor-core
+//     prefill.  The decode items run on the CUDA-core kernel in those two
+//     cases, or when G <= 2 and every small-query request has qo_b == 1;
+//     else on the warp-MMA kernel.  Row class of an item: R_b <= 8, 16, 32
+//     or 64.
 //  3. Decode split ("kv-parallelism" / split-k in the same issue): chunk c0 =
 //     clamp(ceil(P_dec / (4 * SMs)), 256 keys, 2048 keys) in whole pages,
 //     P_dec = sum of decode pages x Hkv.  With N(c) = sum over (request,
@@ -31,7 +33,8 @@
 //     one page.
 //  4. Prefill: items of 256 packed rows = 256/G tokens x G heads of one kv
 //     head, run as two 128-row MMA tiles that share every K/V tile load (as
-//     do the G heads).  An item needs keys [0, kv_b - qo_b + t0 + n) under
+//     do the G heads); at head_dim 256 items of one 128-row tile (two
+//     tiles' accumulators would not fit in tensor memory).  An item needs keys [0, kv_b - qo_b + t0 + n) under
 //     the bottom-right causal mask; key tiles past that are never visited
 //     (the "skips the fully masked out tails" of the llama.cpp discussion
 //     "Pad for prefill stage?").  Split when the
@@ -96,7 +99,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   if (Hq < 1 || Hkv < 1 || Hq % Hkv)
     return fail(err, PA_ERR_INVALID_ARG, "num_qo_heads must be a positive multiple of num_kv_heads");
   const int32_t G = Hq / Hkv;
-  if (D != 64 && D != 128) return fail(err, PA_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (D != 64 && D != 128 && D != 256) return fail(err, PA_ERR_UNSUPPORTED, "head_dim must be 64, 128 or 256");
   if (ps < 1 || ps > 128 || (ps & (ps - 1)))
     return fail(err, PA_ERR_UNSUPPORTED, "page_size must be a power of two in [1, 128]");
   if (in.dtype != PA_FP16 && in.dtype != PA_BF16) return fail(err, PA_ERR_UNSUPPORTED, "dtype");
@@ -173,16 +176,17 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   const int64_t nnz_all = nnz + nnz_pre;
 
   const bool dec_group = (G == 1 || G == 2 || G == 4 || G == 8 || G == 16);
+  const bool cores_only = in.decode_cuda_cores || D == 256;
   std::vector<char> is_dec(B, 0);
   bool multi_tok = false;
   for (int b = 0; b < B; ++b) {
     const int64_t qo = req[b].qo;
     bool d = qo >= 1 && dec_group && !in.force_prefill && qo * G <= kDecMaxRows && (qo == 1 || req[b].kv > kKvTile);
-    if (in.decode_cuda_cores) d = d && qo == 1 && G <= 8;
+    if (cores_only) d = d && qo == 1 && G <= 8;
     is_dec[b] = d ? 1 : 0;
     if (d && qo > 1) multi_tok = true;
   }
-  const int32_t dec_cores = (in.decode_cuda_cores || (G <= 2 && !multi_tok)) ? 1 : 0;
+  const int32_t dec_cores = (cores_only || (G <= 2 && !multi_tok)) ? 1 : 0;
 
   // -- rule 3: decode items
   int64_t p_dec = 0;
@@ -234,7 +238,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   }
 
   // -- rule 4: prefill items
-  const int32_t tq = kItemRows / G;
+  const int32_t tq = (D == 256 ? kQRows : kItemRows) / G;
   struct Tile { int32_t b, t0, n; int64_t e; };
   auto tiles_of = [&](int b, std::vector<Tile>& out) {
     for (int32_t t0 = 0; t0 < req[b].qo; t0 += tq) {

@@ -57,21 +57,26 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <int D>
 struct PreCfg {
   static constexpr int NKB = D / 64;                 // 128-byte column blocks of a row
-  static constexpr int NST = (D == 128) ? 2 : 4;     // K/V pipeline stages
+  // Q tiles per CTA: two, except at D = 256, where O alone takes 256 TMEM
+  // columns a tile (S_A, O_A = 384 of 512 columns; the items are one tile)
+  static constexpr int NT = (D == 256) ? 1 : 2;
+  static constexpr int NST = (D == 128) ? 2 : (D == 64 ? 4 : 1);  // K/V pipeline stages
   static constexpr int BLK = 128 * 128;              // one 128-row x 128-byte block
   static constexpr int Q_BYTES = NKB * BLK;          // one 128-row Q tile
   static constexpr int KV_BYTES = NKB * BLK;         // 128 keys of K (or V)
   static constexpr int P_BYTES = 2 * BLK;            // 128 rows x 128 keys x 2 bytes
   static constexpr int OFF_Q = 0;                    // tiles A, B
-  static constexpr int OFF_K = 2 * Q_BYTES;
+  static constexpr int OFF_K = NT * Q_BYTES;
   static constexpr int OFF_V = OFF_K + NST * KV_BYTES;
   static constexpr int OFF_FREE = OFF_V + NST * KV_BYTES;
   // P_lo buffers for the first key tile: tile A reuses K stage 0 when it is
   // large enough (its keys are consumed by both S MMAs before P is written)
   static constexpr int OFF_PLO_A = (KV_BYTES >= P_BYTES) ? OFF_K : OFF_FREE;
   static constexpr int OFF_PLO_B = (KV_BYTES >= P_BYTES) ? OFF_FREE : OFF_FREE + P_BYTES;
-  static constexpr int OFF_BAR = OFF_PLO_B + P_BYTES;
+  static constexpr int OFF_BAR = (NT == 1) ? OFF_FREE : OFF_PLO_B + P_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + alignment slack
+  static_assert(NT == 2 || KV_BYTES >= P_BYTES, "a one-tile CTA keeps P_lo in K stage 0");
+  static_assert(SMEM <= 232448, "shared memory per CTA");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -138,7 +143,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   const ReqEntry rq = p.req[it.req];
   const int G = p.G;
   const int TQ = kQRows >> p.g_shift;           // tokens per 128-row tile
-  const bool has_b = it.q_ntok > TQ;
+  const bool has_b = C::NT == 2 && it.q_ntok > TQ;
   const int nkt = (it.kv_tok1 - it.kv_tok0 + kKvTile - 1) / kKvTile;
   // split P on the first key tile when some row of the item sees < 128 keys
   const int first_vis = p.causal ? (rq.kv_len - rq.qo_len + it.q_tok0 + 1) : rq.kv_len;
@@ -575,6 +580,9 @@ cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const
   if (a.hp->D == 128)
     return bf ? launch_prefill_t<__nv_bfloat16, 128>(a, m, map_q, kp, use_tma)
               : launch_prefill_t<__half, 128>(a, m, map_q, kp, use_tma);
+  if (a.hp->D == 256)
+    return bf ? launch_prefill_t<__nv_bfloat16, 256>(a, m, map_q, kp, use_tma)
+              : launch_prefill_t<__half, 256>(a, m, map_q, kp, use_tma);
   return bf ? launch_prefill_t<__nv_bfloat16, 64>(a, m, map_q, kp, use_tma)
             : launch_prefill_t<__half, 64>(a, m, map_q, kp, use_tma);
 }

@@ -122,7 +122,10 @@ typedef struct {
  *                  that has pages.
  * num_qo_heads, num_kv_heads: num_qo_heads a positive multiple of num_kv_heads;
  *                  the group size num_qo_heads / num_kv_heads must divide 128.
- * head_dim         64 or 128.  page_size: a power of two in [1, 128].
+ * head_dim         64, 128 or 256 (at 256 decode runs on the CUDA-core kernel
+ *                  for single-token requests at group size <= 8, everything
+ *                  else on the tensor-core prefill kernel).  page_size: a
+ *                  power of two in [1, 128].
  * causal           1: bottom-right causal mask (qo_len <= kv_len required);
  *                  0: every row sees all kv_len keys.
  * workspace        caller-owned device buffer (the wrapper's workspace in the
@@ -291,8 +294,8 @@ PAGEDATTN_API pagedattn_status pagedattn_debug_gather(pagedattn_plan_t plan, int
  *
  * The batch must have no prefill items (every request has qo_len 0 or
  * qo_len * G <= 64 with the group size G = num_qo_heads / num_kv_heads in
- * {1, 2, 4, 8, 16}, and force_prefill is off; with decode_cuda_cores,
- * qo_len <= 1 and G <= 8): PA_ERR_UNSUPPORTED otherwise.  A plan whose metadata and partial
+ * {1, 2, 4, 8, 16}, and force_prefill is off; with decode_cuda_cores or at
+ * head_dim 256, qo_len <= 1 and G <= 8): PA_ERR_UNSUPPORTED otherwise.  A plan whose metadata and partial
  * states exceed 16 MiB returns PA_ERR_WORKSPACE_TOO_SMALL (plan with a larger
  * decode_chunk_pages).  The call allocates no memory.  Its first call on a
  * device looks up the array's device address (cudaGetSymbolAddress) while

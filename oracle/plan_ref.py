@@ -16,11 +16,11 @@ Rules (the planner is deterministic; nothing depends on timing):
    1, 2, 4, 8, 16, the request's R_b = qo_b * G packed (token, head) rows
    number at most 64, a request with qo_b > 1 has kv_b > 128 (more keys
    than one prefill key tile), and ``force_prefill`` is off.  With
-   ``decode_cuda_cores`` only qo_b == 1 at G <= 8 qualifies.  Every other
-   request with qo_b >= 1 goes to the tensor-core prefill kernel.  The
-   decode items run on CUDA cores (header word 29 = 1) when
-   ``decode_cuda_cores`` is set, or when G <= 2 and no small-query request
-   has qo_b > 1; else on the warp-MMA kernel (0).  An item's row class is
+   ``decode_cuda_cores``, or at head_dim 256, only qo_b == 1 at G <= 8
+   qualifies.  Every other request with qo_b >= 1 goes to the tensor-core
+   prefill kernel.  The decode items run on CUDA cores (header word 29 = 1)
+   in those two cases, or when G <= 2 and no small-query request has
+   qo_b > 1; else on the warp-MMA kernel (0).  An item's row class is
    0, 1, 2, 3 for R_b <= 8, 16, 32, 64.
 3. Decode split ("kv-parallelism", the split-k of the same issue): with
    P_dec = sum over decode requests of pages_b * Hkv and
@@ -34,7 +34,7 @@ Rules (the planner is deterministic; nothing depends on timing):
    n = ceil(pages_b / chunk) splits, split s covering pages
    [floor(s * pages_b / n), floor((s + 1) * pages_b / n)), for every kv head.
 4. Prefill items: 256 packed rows = (256 / G) query tokens x G heads (two
-   128-row tiles).  Item [t0, t0 + n) of request b needs keys [0, e) with
+   128-row tiles); at head_dim 256, 128 packed rows (one tile).  Item [t0, t0 + n) of request b needs keys [0, e) with
    e = kv_b - qo_b + t0 + n (causal) or kv_b; that is ceil(e / 128) key
    tiles of 128.  With W = the
    sum of key tiles over all (tile, kv head) items and target = 2 * num_sms,
@@ -118,7 +118,7 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
     if Hq < 1 or Hkv < 1 or Hq % Hkv:
         raise PlanError("num_qo_heads must be a positive multiple of num_kv_heads")
     G = Hq // Hkv
-    if D not in (64, 128):
+    if D not in (64, 128, 256):
         raise Unsupported("head_dim")
     if ps < 1 or ps > 128 or (ps & (ps - 1)):
         raise Unsupported("page_size")
@@ -166,11 +166,11 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
     for (qo, kv, _, _) in lens:
         d = (qo >= 1 and G in DECODE_GROUPS and not force_prefill and qo * G <= DEC_MAX_ROWS
              and (qo == 1 or kv > KV_TILE))
-        if decode_cuda_cores:
+        if decode_cuda_cores or D == 256:
             d = d and qo == 1 and G <= 8
         is_dec.append(d)
     multi = any(d and l[0] > 1 for l, d in zip(lens, is_dec))
-    dec_cores = 1 if (decode_cuda_cores or (G <= 2 and not multi)) else 0
+    dec_cores = 1 if (decode_cuda_cores or D == 256 or (G <= 2 and not multi)) else 0
 
     # -- decode items (rule 3)
     p_dec = sum(l[3] * Hkv for l, d in zip(lens, is_dec) if d)
@@ -205,7 +205,7 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
                 dec.append((b, h, t0, t1, base + s * R if ns > 1 else -1, -1, 0, cls))
 
     # -- prefill items (rule 4)
-    tq = ITEM_ROWS // G
+    tq = (Q_ROWS if D == 256 else ITEM_ROWS) // G
 
     def tiles_of(b):
         qo, kv = lens[b][0], lens[b][1]

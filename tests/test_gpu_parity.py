@@ -197,7 +197,7 @@ def test_device_metadata_equals_restated_plan():
 
 
 @pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
-@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("D", [64, 128, 256])
 @pytest.mark.parametrize("G", [1, 2, 4, 8, 16])
 def test_shapes_groups_dtypes(dtype, D, G):
     Hkv = 2
@@ -311,6 +311,27 @@ def test_many_splits_merge():
     assert_close(out, lse, ro, rl, w.dtype, what="400 splits")
 
 
+D256_CASES = [(16, {}), (1, {}), (16, {"prefill_chunk_tiles": 1, "decode_chunk_pages": 2}),
+              (64, {"force_prefill": True}), (4, {"decode_chunk_pages": 1})]
+
+
+@pytest.mark.parametrize("dtype", [torch.float16, torch.bfloat16])
+@pytest.mark.parametrize("ps,opts", D256_CASES, ids=[f"ps{p}-{'-'.join(map(str, o))}" for p, o in D256_CASES])
+def test_head_dim_256(dtype, ps, opts):
+    """head_dim 256: prefill items of one 128-row tile over several key tiles
+    with a ragged tail (and a request whose rows see fewer than 128 keys),
+    single-token decode on the CUDA-core kernel, a multi-token small request
+    on the prefill kernel, split-KV with the merge, TMA and cp.async pages."""
+    qos, kvs = [1, 300, 1, 5, 130, 0, 40], [1, 300, 700, 400, 900, 17, 60]
+    w = workloads.make_custom("d256", qos, kvs, 8, 2, 256, ps, dtype=dtype, seed=256 + ps + len(opts))
+    ro, rl = A.attention(w)
+    out, lse, plan = run(w, **opts)
+    h = plan_ref.decode_header(plan.dump())
+    if not opts.get("force_prefill"):
+        assert h["dec_cuda_cores"] == 1 and h["n_dec"] > 0 and h["n_pre"] > 0
+    assert_close(out, lse, ro, rl, dtype, what=f"D256 ps{ps} {opts}")
+
+
 def _hnd(kv):
     """The same logical cache in the HND layout [P, 2, Hkv, page_size, D]."""
     return kv.permute(0, 1, 3, 2, 4).contiguous()
@@ -318,7 +339,8 @@ def _hnd(kv):
 
 HND_CASES = [("tiny", {}), ("tiny", {"force_prefill": True}), ("mixed", {}),
              ("mixed", {"decode_chunk_pages": 1, "prefill_chunk_tiles": 1}), ("decode", {"decode_cuda_cores": True}),
-             ("smallq", {}), ("ps1", {}), ("ps128", {}), ("mixed", {"force_cp_async": True})]
+             ("smallq", {}), ("ps1", {}), ("ps128", {}), ("mixed", {"force_cp_async": True}), ("d256", {}),
+             ("d256", {"force_cp_async": True})]
 
 
 @pytest.mark.parametrize("name,opts", HND_CASES, ids=[f"{n}-{'-'.join(map(str, o))}" for n, o in HND_CASES])
@@ -334,6 +356,9 @@ def test_hnd_layout_equals_nhd_bitexact(name, opts):
     elif name == "smallq":
         w = workloads.make_custom("hq", [4, 2, 8, 1], [300, 700, 200, 90], 16, 2, 128, 16, dtype=torch.bfloat16,
                                   seed=31)
+    elif name == "d256":
+        w = workloads.make_custom("h256", [1, 140, 1, 3], [500, 300, 90, 200], 16, 2, 256, 16,
+                                  dtype=torch.bfloat16, seed=33)
     else:
         ps = int(name[2:])
         w = workloads.make_custom("hp", [1, 9, 1, 70], [77, 9, 300, 270], 8, 2, 128, ps, dtype=torch.bfloat16,
@@ -341,7 +366,7 @@ def test_hnd_layout_equals_nhd_bitexact(name, opts):
     o1, l1, _ = run(w, **opts)
     o2, l2, _ = run(w, kv=_hnd(w.kv_cache), kv_layout="HND", **opts)
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
-    if name in ("tiny", "smallq"):
+    if name in ("tiny", "smallq", "d256"):
         ro, rl = A.attention(w)
         assert_close(o2, l2, ro, rl, w.dtype, what=f"HND {name}")
 

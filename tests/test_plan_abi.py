@@ -59,6 +59,7 @@ CASES = [
     ("random", {"decode_cuda_cores": True}), ("smallq", {}), ("smallq", {"decode_cuda_cores": True}),
     ("smallq", {"decode_chunk_pages": 2}), ("smallq_g16", {}), ("smallq_g1", {}), ("specdec", {}),
     ("tiny", {"kv_layout": "HND"}), ("smallq", {"kv_layout": "HND"}),
+    ("d256", {}), ("d256", {"prefill_chunk_tiles": 1, "decode_chunk_pages": 2}), ("d256_g16", {}),
 ]
 
 
@@ -91,6 +92,12 @@ def make(name):
         return workloads.make_custom("sq1", [64, 65, 3, 1], [64, 200, 1000, 9], 2, 2, 64, 4, seed=13)
     if name == "specdec":
         return workloads.mixed(num_decode=24, prefill_len=0, kv_lo=16, kv_hi=3000, decode_qo=4)
+    if name == "d256":  # G 4: decodes, a 5-token request, prefills of 1 and 3 tiles
+        return workloads.make_custom("d256", [1, 300, 1, 5, 130, 0], [1, 300, 700, 400, 900, 17], 8, 2, 256, 16,
+                                     seed=14)
+    if name == "d256_g16":
+        return workloads.make_custom("d256g", [1, 1, 9], [70, 500, 900], 16, 1, 256, 8, dtype=torch.bfloat16,
+                                     seed=15)
     if name == "empty":
         return workloads.make_custom("e", [], [], 4, 1, 64, 16, seed=7)
     if name == "qo0":
@@ -150,6 +157,7 @@ def test_errors_invalid(lib):
 def test_errors_unsupported(lib):
     w = workloads.tiny()
     _expect(pa.PA_ERR_UNSUPPORTED, w, head_dim=96)
+    _expect(pa.PA_ERR_UNSUPPORTED, w, head_dim=512)
     _expect(pa.PA_ERR_UNSUPPORTED, w, page_size=3)
     _expect(pa.PA_ERR_UNSUPPORTED, w, page_size=256)
     _expect(pa.PA_ERR_UNSUPPORTED, w, num_qo_heads=6, num_kv_heads=2)   # group 3 does not divide 128
@@ -240,6 +248,24 @@ def test_plan_small_query_semantics(lib):
     assert hc["dec_cuda_cores"] == 1 and hc["n_pre"] > 0
     hb = plan_ref.decode_header(_lib_blob(b, num_sms=148))
     assert hb["dec_cuda_cores"] == 0 and hb["n_pre"] == 0 and hb["dec_class_items"][0] == hb["n_dec"]
+
+
+def test_plan_head_dim_256_semantics(lib):
+    """At head_dim 256 a prefill item is one 128-row tile, single-token
+    requests at G <= 8 decode on the CUDA-core kernel, and every other
+    request (several tokens, or G = 16) goes to the prefill kernel."""
+    w = make("d256")
+    blob = _lib_blob(w, num_sms=148)
+    h = plan_ref.decode_header(blob)
+    dec, pre, mer = plan_ref.items(blob)
+    assert h["dec_cuda_cores"] == 1
+    assert sorted({int(b) for b in dec[:, 0]}) == [0, 2]          # the two single-token requests
+    assert sorted({int(b) for b in pre[:, 0]}) == [1, 3, 4]       # 5 tokens, 300 and 130 tokens
+    assert pre[:, 3].max() == 32                                  # 32 tokens x 4 heads = one tile
+    r1 = pre[pre[:, 0] == 1]
+    assert len(r1) == 2 * 10 and (r1[:, 3] == 32).sum() == 2 * 9  # 300 tokens: 9 tiles of 32 and one of 12, x 2 kv heads
+    g16 = plan_ref.decode_header(_lib_blob(make("d256_g16"), num_sms=148))
+    assert g16["n_dec"] == 0 and g16["n_pre"] > 0
 
 
 def _cascade_cases():
