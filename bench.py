@@ -524,9 +524,9 @@ def measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, E, world, dev, hdr, popts, p
     value): a serving loop with two steps in flight -- double-buffered
     workspaces and q/out/lse buffers, copies on a second stream -- so that
     step i+1's planning and upload and step i-1's download overlap step i's
-    kernels (uploads and downloads on streams of their own); every step
-    still plans, uploads its q and downloads its out and lse, all inside the
-    timed region."""
+    kernels (uploads, the plan's metadata included, and downloads on
+    streams of their own); every step still plans, uploads its q and
+    downloads its out and lse, all inside the timed region."""
     import torch
     q_h = w.q.pin_memory()
     args_plan = pargs  # the timed plan's arguments (a cascade's own page tables included)
@@ -569,8 +569,12 @@ def measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, E, world, dev, hdr, popts, p
         if sl["plan"] is not None:      # at most two steps in flight: this slot's last run is done
             sl["run"].synchronize()
             sl["plan"].close()
-        plan = pa.Plan(**args_plan, dtype=w.dtype, workspace=sl["ws"], stream=cs, **popts)
-        xs.wait_event(sl["run"])        # the slot's q is free once its last run is done
+        # the slot's workspace and q are free once its last run is done.  The
+        # plan uploads its metadata from pageable memory, which holds the host
+        # until the stream reaches the copy: on the upload stream that is at
+        # once, on the compute stream it would be after the previous step
+        xs.wait_event(sl["run"])
+        plan = pa.Plan(**args_plan, dtype=w.dtype, workspace=sl["ws"], stream=xs, **popts)
         with torch.cuda.stream(xs):
             sl["q"].copy_(q_h, non_blocking=True)
         sl["h2d"].record(xs)
@@ -604,8 +608,9 @@ def measure_e2e(pa, w, q, kv, out, lse, ws, roof_t, E, world, dev, hdr, popts, p
            "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
            "serial_ms_per_step": serial_ms, "serial_value": 100.0 * roof_t / (serial_ms * 1e-3),
            "note": "every step: plan (host) + metadata and q upload from pinned memory + run + out/lse download "
-                   "to pinned memory; two steps in flight (double-buffered workspaces and buffers, copies on a "
-                   "stream each for uploads and downloads); serial_*: one step at a time. The KV cache stays resident"}
+                   "to pinned memory; two steps in flight (double-buffered workspaces and buffers, uploads -- the "
+                   "plan's metadata included -- and downloads on a stream each); serial_*: one step at a time. "
+                   "The KV cache stays resident"}
     return e2e
 
 

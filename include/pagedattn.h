@@ -131,7 +131,12 @@ typedef struct {
  * workspace        caller-owned device buffer (the wrapper's workspace in the
  *                  script); the plan writes its metadata (work items, page ids,
  *                  merge map) to its start with one cudaMemcpyAsync on `stream`
- *                  and keeps fp32 split-KV partial states after it.  It must stay
+ *                  and keeps fp32 split-KV partial states after it.  The copy's
+ *                  source is pageable host memory, so the call may hold the
+ *                  host until `stream` reaches it: a serving loop that plans
+ *                  the next step while the current one runs passes a stream
+ *                  that is not queued behind the running kernels (its upload
+ *                  stream).  It must stay
  *                  allocated and untouched while the plan is used.  NULL builds a
  *                  host-only plan (metadata inspection; run() then fails).
  * workspace_bytes  its size; PA_ERR_WORKSPACE_TOO_SMALL below the size
