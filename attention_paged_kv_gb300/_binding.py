@@ -57,7 +57,7 @@ class Options(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int32), ("force_prefill", ctypes.c_int32),
                 ("decode_chunk_pages", ctypes.c_int32), ("prefill_chunk_tiles", ctypes.c_int32),
                 ("force_cp_async", ctypes.c_int32), ("decode_cuda_cores", ctypes.c_int32),
-                ("kv_layout", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
+                ("kv_layout", ctypes.c_int32), ("prefill_q_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
@@ -174,7 +174,7 @@ def layout_code(layout) -> int:
 
 
 def _options(num_sms=0, force_prefill=False, decode_chunk_pages=0, prefill_chunk_tiles=0,
-             force_cp_async=False, decode_cuda_cores=False, kv_layout="NHD") -> Options:
+             force_cp_async=False, decode_cuda_cores=False, kv_layout="NHD", prefill_q_tiles=0) -> Options:
     o = Options()
     o.num_sms = int(num_sms)
     o.force_prefill = int(bool(force_prefill))
@@ -183,6 +183,7 @@ def _options(num_sms=0, force_prefill=False, decode_chunk_pages=0, prefill_chunk
     o.force_cp_async = int(bool(force_cp_async))
     o.decode_cuda_cores = int(bool(decode_cuda_cores))
     o.kv_layout = layout_code(kv_layout)
+    o.prefill_q_tiles = int(prefill_q_tiles)
     return o
 
 

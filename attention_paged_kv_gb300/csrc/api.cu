@@ -131,12 +131,17 @@ pagedattn_status fill_inputs(pa::PlanInputs* in, const int32_t* qo_indptr, const
     return set_err(PA_ERR_UNSUPPORTED, "kv_layout must be PA_LAYOUT_NHD or PA_LAYOUT_HND");
   if (o.num_sms < 0 || o.decode_chunk_pages < 0 || o.prefill_chunk_tiles < 0)
     return set_err(PA_ERR_INVALID_ARG, "negative option");
+  if (o.prefill_q_tiles < 0 || o.prefill_q_tiles > 2)
+    return set_err(PA_ERR_INVALID_ARG, "prefill_q_tiles must be 0, 1 or 2");
+  if (o.prefill_q_tiles == 2 && head_dim == 256)
+    return set_err(PA_ERR_UNSUPPORTED, "head_dim 256 runs one query tile per prefill item");
   in->num_sms = o.num_sms;
   in->force_prefill = o.force_prefill ? 1 : 0;
   in->decode_chunk_pages = o.decode_chunk_pages;
   in->prefill_chunk_tiles = o.prefill_chunk_tiles;
   in->decode_cuda_cores = o.decode_cuda_cores ? 1 : 0;
   in->kv_layout = o.kv_layout;
+  in->prefill_q_tiles = o.prefill_q_tiles;
   if (in->num_sms == 0) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);

@@ -20,6 +20,7 @@ struct HostPlan {
   int32_t B = 0, Hq = 0, Hkv = 0, D = 0, ps = 0, num_pages = 0, dtype = 0, causal = 1, T = 0, nnz = 0;
   int32_t n_dec = 0, n_pre = 0, n_merge = 0, n_part = 0, G = 1, num_sms = 0;
   int32_t dec_cores = 0;                  // 1: decode items run on the CUDA-core kernel
+  int32_t pre_tiles = 2;                  // 128-row Q tiles per prefill item (1 or 2)
   int32_t hnd = 0;                        // cache layout: 0 NHD, 1 HND
   int32_t n_dec_class[4] = {0, 0, 0, 0};  // decode items per row class, consecutive in item order
   size_t blob_bytes = 0, off_part_o = 0, off_part_lse = 0, total_bytes = 0;
@@ -34,6 +35,7 @@ struct PlanInputs {
   const int32_t* kv_last_page_len;
   int32_t B, Hq, Hkv, D, ps, num_pages, dtype, causal;
   int32_t num_sms, force_prefill, decode_chunk_pages, prefill_chunk_tiles, decode_cuda_cores, kv_layout;
+  int32_t prefill_q_tiles;  // 0: the planner's choice, else 1 or 2 Q tiles per prefill item
   // shared-prefix cascade (n_groups == 0: a plain plan)
   const int32_t* group_indptr;
   const int32_t* prefix_page_indptr;

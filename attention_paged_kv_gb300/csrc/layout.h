@@ -15,11 +15,12 @@ enum HdrIdx : int {
   H_NDEC_CLASS0 = 33,  // decode items per row class (<= 8, 16, 32, 64 rows), in item order
   H_LAYOUT = 37,       // cache layout: 0 NHD, 1 HND
   H_NGROUPS = 38,      // shared-prefix groups (request entries B .. B + groups - 1 are their prefixes)
+  H_PRE_TILES = 39,    // 128-row Q tiles per prefill item (1 or 2)
   HDR_WORDS = 64
 };
 
 constexpr int32_t kMagic = 0x50414731;
-constexpr int32_t kVersion = 4;
+constexpr int32_t kVersion = 5;
 constexpr int kDecClasses = 4;
 constexpr int kDecMaxRows = 64;  // packed (token, head) rows of a small-query item
 constexpr int kQRows = 128;   // packed query rows per prefill MMA tile

@@ -33,8 +33,12 @@
 //     one page.
 //  4. Prefill: items of 256 packed rows = 256/G tokens x G heads of one kv
 //     head, run as two 128-row MMA tiles that share every K/V tile load (as
-//     do the G heads); at head_dim 256 items of one 128-row tile (two
-//     tiles' accumulators would not fit in tensor memory).  An item needs keys [0, kv_b - qo_b + t0 + n) under
+//     do the G heads).  Items of one 128-row tile instead (two CTAs then
+//     share an SM) at head_dim 256 (two tiles' accumulators would not fit
+//     in tensor memory), with prefill_q_tiles = 1, or when most two-tile
+//     items would run only their first tile: with n1 = sum over prefill
+//     requests (and cascade prefixes) of ceil(qo_b / (128/G)) and n2 the
+//     same at 256/G, when 2 * n1 <= 3 * n2.  An item needs keys [0, kv_b - qo_b + t0 + n) under
 //     the bottom-right causal mask; key tiles past that are never visited
 //     (the "skips the fully masked out tails" of the llama.cpp discussion
 //     "Pad for prefill stage?").  Split when the
@@ -238,7 +242,24 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   }
 
   // -- rule 4: prefill items
-  const int32_t tq = (D == 256 ? kQRows : kItemRows) / G;
+  int32_t pre_tiles = 2;
+  if (D == 256) {
+    pre_tiles = 1;
+  } else if (in.prefill_q_tiles > 0) {
+    pre_tiles = in.prefill_q_tiles;
+  } else {  // one tile when most two-tile items would run only their first tile
+    int64_t n1 = 0, n2 = 0;
+    auto count = [&](int64_t qo) {
+      n1 += cdiv(qo, kQRows / G);
+      n2 += cdiv(qo, kItemRows / G);
+    };
+    for (int b = 0; b < B; ++b)
+      if (!is_dec[b] && req[b].qo > 0) count(req[b].qo);
+    for (const Grp& g : grp)
+      if (g.np > 0 && g.T > 0) count(g.T);
+    if (2 * n1 <= 3 * n2) pre_tiles = 1;
+  }
+  const int32_t tq = pre_tiles * kQRows / G;
   struct Tile { int32_t b, t0, n; int64_t e; };
   auto tiles_of = [&](int b, std::vector<Tile>& out) {
     for (int32_t t0 = 0; t0 < req[b].qo; t0 += tq) {
@@ -377,6 +398,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   for (int c = 0; c < kDecClasses; ++c) blob[H_NDEC_CLASS0 + c] = n_class[c];
   blob[H_LAYOUT] = in.kv_layout;
   blob[H_NGROUPS] = NG;
+  blob[H_PRE_TILES] = pre_tiles;
   if (nnz) std::memcpy(blob.data() + off_pages / 4, in.kv_page_indices, size_t(4 * nnz));
   if (nnz_pre) std::memcpy(blob.data() + off_pages / 4 + nnz, in.prefix_page_indices, size_t(4 * nnz_pre));
   for (int b = 0; b < B; ++b) {
@@ -412,6 +434,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   hp->n_dec = int32_t(dec.size()); hp->n_pre = int32_t(pre.size()); hp->n_merge = int32_t(merges.size());
   hp->n_part = int32_t(part); hp->G = G; hp->num_sms = in.num_sms;
   hp->dec_cores = dec_cores;
+  hp->pre_tiles = pre_tiles;
   hp->hnd = in.kv_layout;
   for (int c = 0; c < kDecClasses; ++c) hp->n_dec_class[c] = n_class[c];
   hp->blob_bytes = size_t(blob_bytes); hp->off_part_o = size_t(off_part_o);

@@ -27,6 +27,11 @@
 // 384 (fp32 128xD).  P (fp16/bf16, two per column) is written over the first
 // 64 columns of its S and feeds the PV MMA as a TMEM A operand.
 //
+// The one-tile variant (template NT = 1: 128-row items, 192 threads, S at
+// TMEM column 0 and O at 128, one K/V stage) serves head_dim 256, whose O
+// takes 256 columns a tile, and batches of short prompts, where two CTAs to
+// an SM hide each other's fixed costs (Q and first K/V loads, epilogue).
+//
 // Per key tile j the MMA thread issues, in order:
 //   PV_A(j) ; S_A(j+1) ; PV_B(j) ; S_B(j+1)
 // so while the softmax warps of one tile turn S into P, the tensor core works
@@ -50,17 +55,19 @@
 namespace pa {
 namespace {
 
-constexpr int kPreThreads = 320;
-constexpr uint32_t kTmemCols = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 
-template <int D>
+// NT = 128-row Q tiles per CTA.  Two tiles (the default) share every K/V
+// load and take turns on the tensor core; one tile at D = 256, where O alone
+// takes 256 TMEM columns a tile, and for batches of short prompts, where one
+// tile per CTA lets two CTAs share an SM and hide each other's fixed costs.
+template <int D, int NT>
 struct PreCfg {
+  static_assert(NT == 1 || (NT == 2 && D <= 128), "two tiles need 2 x (128 + D) <= 512 TMEM columns");
+  static constexpr int THREADS = 32 * (4 * NT + 2);  // softmax warpgroup(s), producer, MMA issuer
+  static constexpr int WARP_PROD = 4 * NT, WARP_MMA = 4 * NT + 1;
   static constexpr int NKB = D / 64;                 // 128-byte column blocks of a row
-  // Q tiles per CTA: two, except at D = 256, where O alone takes 256 TMEM
-  // columns a tile (S_A, O_A = 384 of 512 columns; the items are one tile)
-  static constexpr int NT = (D == 256) ? 1 : 2;
-  static constexpr int NST = (D == 128) ? 2 : (D == 64 ? 4 : 1);  // K/V pipeline stages
+  static constexpr int NST = NT == 1 ? 1 : (D == 128 ? 2 : 4);  // K/V pipeline stages
   static constexpr int BLK = 128 * 128;              // one 128-row x 128-byte block
   static constexpr int Q_BYTES = NKB * BLK;          // one 128-row Q tile
   static constexpr int KV_BYTES = NKB * BLK;         // 128 keys of K (or V)
@@ -73,10 +80,14 @@ struct PreCfg {
   // large enough (its keys are consumed by both S MMAs before P is written)
   static constexpr int OFF_PLO_A = (KV_BYTES >= P_BYTES) ? OFF_K : OFF_FREE;
   static constexpr int OFF_PLO_B = (KV_BYTES >= P_BYTES) ? OFF_FREE : OFF_FREE + P_BYTES;
-  static constexpr int OFF_BAR = (NT == 1) ? OFF_FREE : OFF_PLO_B + P_BYTES;
+  static constexpr int OFF_BAR = (NT == 1) ? (OFF_PLO_A == OFF_FREE ? OFF_FREE + P_BYTES : OFF_FREE)
+                                           : OFF_PLO_B + P_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;  // barriers + alignment slack
-  static_assert(NT == 2 || KV_BYTES >= P_BYTES, "a one-tile CTA keeps P_lo in K stage 0");
+  // TMEM: S_x at columns 128 x, O_x after the S columns
+  static constexpr int O_COL = NT * 128;
+  static constexpr uint32_t TMEM_COLS = (NT * (128 + D) <= 256) ? 256u : 512u;
   static_assert(SMEM <= 232448, "shared memory per CTA");
+  static_assert(NT == 2 || D == 256 || 2 * (SMEM + 1024) <= 233472, "two one-tile CTAs share an SM");
 };
 
 __device__ __forceinline__ float ex2(float x) {
@@ -108,11 +119,11 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return r;
 }
 
-template <typename T, int D>
-__global__ void __launch_bounds__(kPreThreads, 1)
+template <typename T, int D, int NT>
+__global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
                    const KParams p, const int use_tma) {
-  using C = PreCfg<D>;
+  using C = PreCfg<D, NT>;
   constexpr int NKB = C::NKB, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw_addr = smem_u32(smem_raw);
@@ -143,7 +154,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   const ReqEntry rq = p.req[it.req];
   const int G = p.G;
   const int TQ = kQRows >> p.g_shift;           // tokens per 128-row tile
-  const bool has_b = C::NT == 2 && it.q_ntok > TQ;
+  const bool has_b = NT == 2 && it.q_ntok > TQ;
   const int nkt = (it.kv_tok1 - it.kv_tok0 + kKvTile - 1) / kKvTile;
   // split P on the first key tile when some row of the item sees < 128 keys
   const int first_vis = p.causal ? (rq.kv_len - rq.qo_len + it.q_tok0 + 1) : rq.kv_len;
@@ -166,13 +177,13 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     *abort_flag = 0;
     mbar_init_fence();
   }
-  if (warp == 9) tmem_alloc(tmem_slot, kTmemCols);
+  if (warp == C::WARP_MMA) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == C::WARP_PROD) {
     // ---------------------------------------------------------------- producer
     if (lane == 0) {
       tma_prefetch_desc(&q_map);
@@ -263,7 +274,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
       }
     }
     __syncwarp();
-  } else if (warp == 9) {
+  } else if (warp == C::WARP_MMA) {
     // ---------------------------------------------------------------- MMA issuer
     if (lane == 0) {
       const uint32_t id_s = idesc_f16(Elt<T>::kBf16, 0, 0, 128, 128);
@@ -279,7 +290,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
         tc_commit(&s_full[x]);
       };
       auto issue_pv = [&](int x, int j, int st) {
-        const uint32_t d = tmem + 256 + x * 128;
+        const uint32_t d = tmem + C::O_COL + x * 128;
 #pragma unroll
         for (int k = 0; k < kKvTile / 16; ++k)
           tc_mma_ts(d, tmem + x * 128 + k * 8, smem_desc_sw128(v_addr(st) + k * 2048, C::BLK, 1024), id_o,
@@ -354,7 +365,7 @@ __global__ void __launch_bounds__(kPreThreads, 1)
     const float sl2 = p.scale_log2;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_col = tmem + lane_base + x * 128;
-    const uint32_t o_col = tmem + lane_base + 256 + x * 128;
+    const uint32_t o_col = tmem + lane_base + C::O_COL + x * 128;
     float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = (x == 0) || has_b;
 
@@ -544,24 +555,39 @@ __global__ void __launch_bounds__(kPreThreads, 1)
   // ---------------------------------------------------------------- teardown
   tc_fence_before();
   __syncthreads();
-  if (warp == 9) {
+  if (warp == C::WARP_MMA) {
     tc_fence_after();
-    tmem_dealloc(tmem, kTmemCols);
+    tmem_dealloc(tmem, C::TMEM_COLS);
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, int NT>
 cudaError_t launch_prefill_t(const RunArgs& a, const CUtensorMap* kv_map, const CUtensorMap* q_map,
                              const KParams& kp, int use_tma) {
-  using C = PreCfg<D>;
+  using C = PreCfg<D, NT>;
   static bool attr_set = false;
   if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(prefill_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel<T, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  prefill_kernel<T, D><<<a.hp->n_pre, kPreThreads, C::SMEM, a.stream>>>(*kv_map, *q_map, kp, use_tma);
+  prefill_kernel<T, D, NT><<<a.hp->n_pre, C::THREADS, C::SMEM, a.stream>>>(*kv_map, *q_map, kp, use_tma);
   return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t launch_prefill_dt(const RunArgs& a, const CUtensorMap* kv_map, const CUtensorMap* q_map,
+                              const KParams& kp, int use_tma) {
+  const bool one = a.hp->pre_tiles == 1;
+  switch (a.hp->D) {
+    case 64: return one ? launch_prefill_t<T, 64, 1>(a, kv_map, q_map, kp, use_tma)
+                        : launch_prefill_t<T, 64, 2>(a, kv_map, q_map, kp, use_tma);
+    case 128: return one ? launch_prefill_t<T, 128, 1>(a, kv_map, q_map, kp, use_tma)
+                         : launch_prefill_t<T, 128, 2>(a, kv_map, q_map, kp, use_tma);
+    case 256: return one ? launch_prefill_t<T, 256, 1>(a, kv_map, q_map, kp, use_tma) : cudaErrorInvalidValue;
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace
@@ -576,15 +602,8 @@ cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const
   CUtensorMap dummy;
   memset(&dummy, 0, sizeof(dummy));
   const CUtensorMap* m = use_tma ? map_sw128 : &dummy;
-  const bool bf = a.hp->dtype == PA_BF16;
-  if (a.hp->D == 128)
-    return bf ? launch_prefill_t<__nv_bfloat16, 128>(a, m, map_q, kp, use_tma)
-              : launch_prefill_t<__half, 128>(a, m, map_q, kp, use_tma);
-  if (a.hp->D == 256)
-    return bf ? launch_prefill_t<__nv_bfloat16, 256>(a, m, map_q, kp, use_tma)
-              : launch_prefill_t<__half, 256>(a, m, map_q, kp, use_tma);
-  return bf ? launch_prefill_t<__nv_bfloat16, 64>(a, m, map_q, kp, use_tma)
-            : launch_prefill_t<__half, 64>(a, m, map_q, kp, use_tma);
+  return a.hp->dtype == PA_BF16 ? launch_prefill_dt<__nv_bfloat16>(a, m, map_q, kp, use_tma)
+                                 : launch_prefill_dt<__half>(a, m, map_q, kp, use_tma);
 }
 
 }  // namespace pa

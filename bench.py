@@ -302,6 +302,7 @@ def main():
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--decode-chunk-pages", type=int, default=0, help="planner override (0: the plan's rule)")
     ap.add_argument("--prefill-chunk-tiles", type=int, default=0, help="planner override (0: the plan's rule)")
+    ap.add_argument("--prefill-q-tiles", type=int, default=0, help="planner override (0: the plan's rule)")
     ap.add_argument("--workload", default="mixed", choices=list(WORKLOADS),
                     help="mixed is the benchmark; the others exist for profiling captures")
     args = ap.parse_args()
@@ -360,7 +361,8 @@ def main():
     lse = torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
-    popts = {"decode_chunk_pages": args.decode_chunk_pages, "prefill_chunk_tiles": args.prefill_chunk_tiles}
+    popts = {"decode_chunk_pages": args.decode_chunk_pages, "prefill_chunk_tiles": args.prefill_chunk_tiles,
+             "prefill_q_tiles": args.prefill_q_tiles}
     pargs = w.plan_args()
     if args.workload in CASCADE:
         groups, pargs = workloads.split_prefix(w, *CASCADE[args.workload])

@@ -86,6 +86,9 @@ typedef struct {
                                   requests all go to the prefill kernel (default:
                                   the warp-MMA small-query kernel, see plan)        */
   int32_t kv_layout;           /* PA_LAYOUT_NHD (default) or PA_LAYOUT_HND: see below */
+  int32_t prefill_q_tiles;     /* 128-row query tiles per prefill work item: 1 or 2;
+                                  0 = the planner's choice (see plan).  head_dim 256
+                                  takes 1 only                                      */
   int32_t reserved[1];         /* must be 0                                          */
 } pagedattn_options;
 

@@ -34,7 +34,11 @@ Rules (the planner is deterministic; nothing depends on timing):
    n = ceil(pages_b / chunk) splits, split s covering pages
    [floor(s * pages_b / n), floor((s + 1) * pages_b / n)), for every kv head.
 4. Prefill items: 256 packed rows = (256 / G) query tokens x G heads (two
-   128-row tiles); at head_dim 256, 128 packed rows (one tile).  Item [t0, t0 + n) of request b needs keys [0, e) with
+   128-row tiles); 128 packed rows (one tile) at head_dim 256, with
+   ``prefill_q_tiles`` = 1, or when n1 = sum over prefill requests (and
+   cascade prefixes, of T_g tokens) of ceil(qo_b / (128 / G)) and n2, the
+   same at 256 / G, satisfy 2 * n1 <= 3 * n2 (most two-tile items would run
+   only their first tile).  Item [t0, t0 + n) of request b needs keys [0, e) with
    e = kv_b - qo_b + t0 + n (causal) or kv_b; that is ceil(e / 128) key
    tiles of 128.  With W = the
    sum of key tiles over all (tile, kv head) items and target = 2 * num_sms,
@@ -62,7 +66,8 @@ start of the workspace:
                 off_pages, off_req, off_dec, off_pre, off_merge, blob_bytes,
                 off_part_o, off_part_lse, total_bytes, dec_cuda_cores, 0, 0,
                 [32] status word, [33..36] decode items per row class,
-                [37] cache layout (0 NHD, 1 HND), [38] shared-prefix groups, 0...
+                [37] cache layout (0 NHD, 1 HND), [38] shared-prefix groups,
+                [39] 128-row query tiles per prefill item, 0...
     pages[nnz]       copy of kv_page_indices
     req[B + groups][4]  qo_start, qo_len, kv_len, page_start (group g's prefix: entry B + g,
                      qo_len 0, its query tokens' qo_start, the prefix pages after the requests')
@@ -77,7 +82,7 @@ import numpy as np
 from .attention import PlanError, request_lengths
 
 MAGIC = 0x50414731
-VERSION = 4
+VERSION = 5
 HDR_WORDS = 64
 STATUS_WORD = 32
 Q_ROWS = 128       # packed query rows per prefill MMA tile (G must divide it)
@@ -110,7 +115,7 @@ def _align(x, a=256):
 def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_heads,
           num_kv_heads, head_dim, page_size, num_pages, dtype=BF16, causal=True, num_sms=148,
           force_prefill=False, decode_chunk_pages=0, prefill_chunk_tiles=0, decode_cuda_cores=False,
-          kv_layout="NHD", prefix_groups=None):
+          kv_layout="NHD", prefix_groups=None, prefill_q_tiles=0):
     """Return the metadata blob (np.int32) the planner must produce.
     ``prefix_groups`` = (group_indptr, prefix_page_indptr, prefix_page_indices)
     plans a shared-prefix cascade (rule 7)."""
@@ -205,7 +210,17 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
                 dec.append((b, h, t0, t1, base + s * R if ns > 1 else -1, -1, 0, cls))
 
     # -- prefill items (rule 4)
-    tq = (Q_ROWS if D == 256 else ITEM_ROWS) // G
+    if D == 256:
+        pre_tiles = 1
+    elif prefill_q_tiles:
+        pre_tiles = int(prefill_q_tiles)
+    else:   # one tile when most two-tile items would run only their first tile
+        qos = [l[0] for l, d in zip(lens, is_dec) if not d and l[0] > 0]
+        qos += [g[2] for g in groups if g[3] > 0 and g[2] > 0]
+        n1 = sum(_cdiv(q, Q_ROWS // G) for q in qos)
+        n2 = sum(_cdiv(q, ITEM_ROWS // G) for q in qos)
+        pre_tiles = 1 if 2 * n1 <= 3 * n2 else 2
+    tq = pre_tiles * Q_ROWS // G
 
     def tiles_of(b):
         qo, kv = lens[b][0], lens[b][1]
@@ -326,6 +341,7 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
     blob[33:33 + len(n_class)] = n_class
     blob[37] = {"NHD": 0, "HND": 1}[kv_layout] if isinstance(kv_layout, str) else int(kv_layout)
     blob[38] = NG
+    blob[39] = pre_tiles
     blob[off_pages // 4: off_pages // 4 + nnz] = indices
     blob[off_pages // 4 + nnz: off_pages // 4 + nnz_all] = pindices
     req = np.array([(int(qo_indptr[b]), qo, kv, p0) for b, (qo, kv, p0, _) in enumerate(lens)],
@@ -349,7 +365,7 @@ def decode_header(blob: np.ndarray) -> dict:
              "off_merge", "blob_bytes", "off_part_o", "off_part_lse", "total_bytes", "dec_cuda_cores"]
     h = {n: int(blob[i]) for i, n in enumerate(names)}
     h["dec_class_items"] = [int(x) for x in blob[33:33 + len(DEC_CLASS_ROWS)]]
-    h["kv_layout"], h["n_groups"] = int(blob[37]), int(blob[38])
+    h["kv_layout"], h["n_groups"], h["pre_tiles"] = int(blob[37]), int(blob[38]), int(blob[39])
     return h
 
 

@@ -311,6 +311,31 @@ def test_many_splits_merge():
     assert_close(out, lse, ro, rl, w.dtype, what="400 splits")
 
 
+ONE_TILE = ["tiny", "ragged", "mixed_small", "prefix", "d64_ps1"]
+
+
+@pytest.mark.parametrize("name", ONE_TILE)
+def test_one_tile_prefill_items(name):
+    """prefill_q_tiles = 1: prefill items of one 128-row tile, two CTAs to an
+    SM (TMA and cp.async pages, head_dim 64 and 128, split-KV)."""
+    if name == "tiny":
+        w = workloads.tiny()
+    elif name == "ragged":
+        w = workloads.ragged()
+    elif name == "mixed_small":
+        w = workloads.mixed(num_decode=24, prefill_len=700, kv_lo=16, kv_hi=3000)
+    elif name == "prefix":
+        w = workloads.prefix()
+    else:
+        w = workloads.make_custom("o64", [1, 90, 300, 7], [40, 90, 800, 200], 8, 2, 64, 1, dtype=torch.bfloat16,
+                                  seed=41)
+    ro, rl = A.attention(w)
+    for opts in ({"prefill_q_tiles": 1}, {"prefill_q_tiles": 1, "prefill_chunk_tiles": 1, "force_prefill": True}):
+        out, lse, plan = run(w, **opts)
+        assert plan_ref.decode_header(plan.dump())["pre_tiles"] == 1
+        assert_close(out, lse, ro, rl, w.dtype, what=f"one tile {name} {opts}")
+
+
 D256_CASES = [(16, {}), (1, {}), (16, {"prefill_chunk_tiles": 1, "decode_chunk_pages": 2}),
               (64, {"force_prefill": True}), (4, {"decode_chunk_pages": 1})]
 

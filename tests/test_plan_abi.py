@@ -60,6 +60,7 @@ CASES = [
     ("smallq", {"decode_chunk_pages": 2}), ("smallq_g16", {}), ("smallq_g1", {}), ("specdec", {}),
     ("tiny", {"kv_layout": "HND"}), ("smallq", {"kv_layout": "HND"}),
     ("d256", {}), ("d256", {"prefill_chunk_tiles": 1, "decode_chunk_pages": 2}), ("d256_g16", {}),
+    ("ragged", {"prefill_q_tiles": 1}), ("tiny", {"prefill_q_tiles": 1}), ("mixed_small", {"prefill_q_tiles": 2}),
 ]
 
 
@@ -158,6 +159,8 @@ def test_errors_unsupported(lib):
     w = workloads.tiny()
     _expect(pa.PA_ERR_UNSUPPORTED, w, head_dim=96)
     _expect(pa.PA_ERR_UNSUPPORTED, w, head_dim=512)
+    _expect(pa.PA_ERR_INVALID_ARG, w, prefill_q_tiles=3)
+    _expect(pa.PA_ERR_UNSUPPORTED, make("d256"), prefill_q_tiles=2)
     _expect(pa.PA_ERR_UNSUPPORTED, w, page_size=3)
     _expect(pa.PA_ERR_UNSUPPORTED, w, page_size=256)
     _expect(pa.PA_ERR_UNSUPPORTED, w, num_qo_heads=6, num_kv_heads=2)   # group 3 does not divide 128
