@@ -81,6 +81,12 @@ def pin_sdpa_contiguous():
                 ro, rl = dense_reference(ww)
                 rows = np.repeat(ww.qo_lens() > 0, ww.qo_lens())
                 ok &= close(o[rows], ro[rows]) and close(l[rows], rl[rows])
+    # head_dim 256 (scale 1/16), pages of 4 slots
+    w3 = workloads.make_custom("c256", [1, 4, 0, 7], [9, 6, 3, 7], 4, 2, 256, 4, seed=19)
+    o, l = A.attention(w3)
+    ro, rl = dense_reference(w3)
+    rows = np.repeat(w3.qo_lens() > 0, w3.qo_lens())
+    ok &= close(o[rows], ro[rows]) and close(l[rows], rl[rows])
     return bool(ok)
 
 
@@ -329,10 +335,14 @@ def test_planted_mistakes(name, monkeypatch):
     ("tiny", 148, {}), ("tiny", 2, {"prefill_chunk_tiles": 1}), ("decode", 148, {}),
     ("ragged", 148, {}), ("prefix", 148, {}), ("tiny", 148, {"force_prefill": True}),
     ("custom_long", 4, {}), ("smallq", 4, {}), ("smallq", 148, {"decode_cuda_cores": True}),
-    ("smallq_g16", 148, {}), ("smallq_g1", 3, {}),
+    ("smallq_g16", 148, {}), ("smallq_g1", 3, {}), ("d256", 148, {}), ("d256", 3, {"decode_chunk_pages": 2}),
+    ("ragged", 148, {"prefill_q_tiles": 1}), ("custom_long", 4, {"prefill_q_tiles": 1}),
+    ("custom_long", 4, {"prefill_q_tiles": 2}),
 ])
 def test_plan_ref_covers_every_pair_once(wname, sms, kw):
-    if wname == "custom_long":
+    if wname == "d256":  # G 4 at head_dim 256: one-token decodes, a 5-token request, 1- and 3-tile prefills
+        w = small([1, 70, 1, 5, 100], [1, 70, 300, 200, 400], 8, 2, D=256, ps=8, seed=7)
+    elif wname == "custom_long":
         w = small([1, 40, 1, 300], [2000, 700, 33, 300], 8, 2, D=64, ps=16, seed=3)
     elif wname == "smallq":  # G 8: rows 32, 32, 16, 8, 64, and a prefill of 9 tokens
         w = small([4, 4, 2, 1, 8, 9], [300, 40, 900, 70, 500, 9], 16, 2, D=64, ps=16, seed=4)

@@ -271,6 +271,25 @@ def test_plan_head_dim_256_semantics(lib):
     assert g16["n_dec"] == 0 and g16["n_pre"] > 0
 
 
+def test_plan_one_tile_rule(lib):
+    """Prefill items of one 128-row tile when most two-tile items would run
+    only their first tile (2 n1 <= 3 n2 with n1, n2 the item counts at 128
+    and 256 rows): the prefix batch (30 tokens x G 4 = 120 rows a request)
+    and the tiny batch take one tile, the ragged and mixed batches two; the
+    option overrides the rule, and head_dim 256 always takes one."""
+    def tiles(w, **kw):
+        return plan_ref.decode_header(_lib_blob(w, num_sms=148, **kw))["pre_tiles"]
+    assert tiles(workloads.prefix()) == 1 and tiles(workloads.tiny()) == 1
+    assert tiles(workloads.ragged()) == 2 and tiles(make("mixed_small")) == 2
+    assert tiles(workloads.ragged(), prefill_q_tiles=1) == 1 and tiles(workloads.prefix(), prefill_q_tiles=2) == 2
+    assert tiles(make("d256")) == 1
+    # the rule at its edge: G 4 (32 tokens a tile), one request of 64 tokens -> n1 2, n2 1: two tiles;
+    # two requests of 32 -> n1 2, n2 2: one tile
+    a = workloads.make_custom("e1", [64], [64], 8, 2, 128, 16, seed=1)
+    b = workloads.make_custom("e2", [32, 32], [32, 32], 8, 2, 128, 16, seed=1)
+    assert tiles(a) == 2 and tiles(b) == 1
+
+
 def _cascade_cases():
     """(name, workload, group_indptr, prefix pages per group)."""
     pre = workloads.prefix()                                    # 64 requests share 12 full pages
