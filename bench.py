@@ -94,13 +94,16 @@ def accounting(w):
     (requests the planner gives to the tcgen05 prefill kernel) and the decode
     part (single-token and small-query requests: qo_len * G <= 64 packed rows
     at a group size G of 1, 2, 4, 8 or 16, and more than 128 keys when
-    qo_len > 1 -- the planner's rule)."""
+    qo_len > 1; at head_dim 256 single-token requests at G <= 8 only -- the
+    planner's rule)."""
     qo = np.diff(w.qo_indptr).astype(np.int64)
     kv = np.asarray(w.gen_kv_lens, np.int64)
     npg = np.diff(w.kv_page_indptr).astype(np.int64)
     D, Hq, Hkv, e = w.head_dim, w.num_qo_heads, w.num_kv_heads, 2
     G = Hq // Hkv
     small = (qo >= 1) & (qo * G <= 64) & (G in (1, 2, 4, 8, 16)) & ((qo == 1) | (kv > 128))
+    if D == 256:
+        small &= (qo == 1) & (G <= 8)
     res = {}
     for part, sel in (("prefill", (qo >= 1) & ~small), ("decode", small)):
         T = int(qo[sel].sum())
