@@ -44,7 +44,8 @@ DEFAULT_WORKSPACE_BYTES = 128 * 1024 * 1024  # the timing script's workspace siz
 EXPORTED = ("pagedattn_plan", "pagedattn_workspace_size", "pagedattn_run", "pagedattn_run_stages",
             "pagedattn_plan_destroy", "pagedattn_last_error", "pagedattn_device_status",
             "pagedattn_debug_plan_dump", "pagedattn_debug_gather", "pagedattn_version",
-            "pagedattn_run_decode_noalloc", "pagedattn_plan_cascade", "pagedattn_workspace_size_cascade")
+            "pagedattn_run_decode_noalloc", "pagedattn_noalloc_device_status", "pagedattn_plan_cascade",
+            "pagedattn_workspace_size_cascade")
 
 
 class PagedAttnError(RuntimeError):
@@ -57,7 +58,8 @@ class Options(ctypes.Structure):
     _fields_ = [("num_sms", ctypes.c_int32), ("force_prefill", ctypes.c_int32),
                 ("decode_chunk_pages", ctypes.c_int32), ("prefill_chunk_tiles", ctypes.c_int32),
                 ("force_cp_async", ctypes.c_int32), ("decode_cuda_cores", ctypes.c_int32),
-                ("kv_layout", ctypes.c_int32), ("prefill_q_tiles", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
+                ("kv_layout", ctypes.c_int32), ("prefill_q_tiles", ctypes.c_int32),
+                ("wait_limit_cycles", ctypes.c_int32), ("reserved", ctypes.c_int32 * 1)]
 
 
 _I32P = ctypes.POINTER(ctypes.c_int32)
@@ -122,6 +124,8 @@ def load() -> ctypes.CDLL:
         lib.pagedattn_debug_gather.restype = ctypes.c_int
         lib.pagedattn_run_decode_noalloc.argtypes = [ctypes.c_void_p] * 6
         lib.pagedattn_run_decode_noalloc.restype = ctypes.c_int
+        lib.pagedattn_noalloc_device_status.argtypes = [ctypes.c_void_p, _I32P]
+        lib.pagedattn_noalloc_device_status.restype = ctypes.c_int
         lib.pagedattn_version.argtypes = []
         lib.pagedattn_version.restype = ctypes.c_char_p
         _lib = lib
@@ -174,7 +178,8 @@ def layout_code(layout) -> int:
 
 
 def _options(num_sms=0, force_prefill=False, decode_chunk_pages=0, prefill_chunk_tiles=0,
-             force_cp_async=False, decode_cuda_cores=False, kv_layout="NHD", prefill_q_tiles=0) -> Options:
+             force_cp_async=False, decode_cuda_cores=False, kv_layout="NHD", prefill_q_tiles=0,
+             wait_limit_cycles=0) -> Options:
     o = Options()
     o.num_sms = int(num_sms)
     o.force_prefill = int(bool(force_prefill))
@@ -184,6 +189,7 @@ def _options(num_sms=0, force_prefill=False, decode_chunk_pages=0, prefill_chunk
     o.decode_cuda_cores = int(bool(decode_cuda_cores))
     o.kv_layout = layout_code(kv_layout)
     o.prefill_q_tiles = int(prefill_q_tiles)
+    o.wait_limit_cycles = int(wait_limit_cycles)
     return o
 
 

@@ -127,6 +127,7 @@ pagedattn_status fill_inputs(pa::PlanInputs* in, const int32_t* qo_indptr, const
   std::memset(&o, 0, sizeof(o));
   if (opts) o = *opts;
   if (o.reserved[0] != 0) return set_err(PA_ERR_INVALID_ARG, "pagedattn_options.reserved must be zero");
+  if (o.wait_limit_cycles < 0) return set_err(PA_ERR_INVALID_ARG, "wait_limit_cycles must be >= 0");
   if (o.kv_layout != PA_LAYOUT_NHD && o.kv_layout != PA_LAYOUT_HND)
     return set_err(PA_ERR_UNSUPPORTED, "kv_layout must be PA_LAYOUT_NHD or PA_LAYOUT_HND");
   if (o.num_sms < 0 || o.decode_chunk_pages < 0 || o.prefill_chunk_tiles < 0)
@@ -142,6 +143,7 @@ pagedattn_status fill_inputs(pa::PlanInputs* in, const int32_t* qo_indptr, const
   in->decode_cuda_cores = o.decode_cuda_cores ? 1 : 0;
   in->kv_layout = o.kv_layout;
   in->prefill_q_tiles = o.prefill_q_tiles;
+  in->wait_limit_cycles = o.wait_limit_cycles;
   if (in->num_sms == 0) {
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -191,6 +193,7 @@ KParams make_params(const RunArgs& a) {
   k.hnd = hp.hnd;
   k.num_pages = hp.num_pages;
   k.scale_log2 = float(1.4426950408889634 / std::sqrt(double(hp.D)));
+  k.wait_limit = hp.wait_limit_cycles > 0 ? (long long)hp.wait_limit_cycles : PA_WAIT_LIMIT_CYCLES;
   return k;
 }
 
@@ -198,7 +201,7 @@ KParams make_params(const RunArgs& a) {
 
 extern "C" {
 
-const char* pagedattn_version(void) { return "0.1.0"; }
+const char* pagedattn_version(void) { return "0.2.0"; }
 
 const char* pagedattn_last_error(void) { return g_last_error.c_str(); }
 
@@ -319,20 +322,32 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
   if (e != cudaSuccess) return cuda_err(e, "cudaGetDevice");
   if (dev != plan->device) return set_err(PA_ERR_INVALID_ARG, "current device differs from the plan's device");
 
-  if ((hp.n_pre > 0 || hp.n_dec > 0) && kv_cache != plan->map_kv) {
-    if (hp.ps >= 8) {
-      pagedattn_status s = encode_kv_map(&plan->map_rows, hp, kv_cache, 64, uint32_t(hp.ps < 64 ? hp.ps : 64),
-                                         CU_TENSOR_MAP_SWIZZLE_128B);
-      if (s != PA_OK) return s;
-      s = encode_kv_map(&plan->map_sw128, hp, kv_cache, 64, uint32_t(hp.ps), CU_TENSOR_MAP_SWIZZLE_128B);
-      if (s != PA_OK) return s;
+  // the tensor maps of the last pointers seen are cached in the plan; the
+  // launches below use copies taken under the plan's lock, so host threads
+  // that run one plan at once never see a half-written map
+  CUtensorMap map_rows, map_sw128, map_q;
+  {
+    std::lock_guard<std::mutex> lock(plan->maps_mu);
+    if ((hp.n_pre > 0 || hp.n_dec > 0) && kv_cache != plan->map_kv) {
+      plan->map_kv = nullptr;
+      if (hp.ps >= 8) {
+        pagedattn_status s = encode_kv_map(&plan->map_rows, hp, kv_cache, 64, uint32_t(hp.ps < 64 ? hp.ps : 64),
+                                           CU_TENSOR_MAP_SWIZZLE_128B);
+        if (s != PA_OK) return s;
+        s = encode_kv_map(&plan->map_sw128, hp, kv_cache, 64, uint32_t(hp.ps), CU_TENSOR_MAP_SWIZZLE_128B);
+        if (s != PA_OK) return s;
+      }
+      plan->map_kv = kv_cache;
     }
-    plan->map_kv = kv_cache;
-  }
-  if (hp.n_pre > 0 && q != plan->map_q_ptr) {
-    pagedattn_status s = pa::encode_q_map(&plan->map_q, hp, q);
-    if (s != PA_OK) return s;
-    plan->map_q_ptr = q;
+    if (hp.n_pre > 0 && q != plan->map_q_ptr) {
+      plan->map_q_ptr = nullptr;
+      pagedattn_status s = pa::encode_q_map(&plan->map_q, hp, q);
+      if (s != PA_OK) return s;
+      plan->map_q_ptr = q;
+    }
+    map_rows = plan->map_rows;
+    map_sw128 = plan->map_sw128;
+    map_q = plan->map_q;
   }
   pa::RunArgs a;
   a.hp = &hp;
@@ -344,11 +359,11 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.force_cp_async = plan->force_cp_async;
   if (stage_mask & PA_STAGE_PREFILL) {
-    e = pa::launch_prefill(a, hp.ps >= 8 ? &plan->map_sw128 : nullptr, &plan->map_q);
+    e = pa::launch_prefill(a, hp.ps >= 8 ? &map_sw128 : nullptr, &map_q);
     if (e != cudaSuccess) return cuda_err(e, "prefill launch");
   }
   if (stage_mask & PA_STAGE_DECODE) {
-    e = pa::launch_decode(a, hp.ps >= 8 ? &plan->map_rows : nullptr);
+    e = pa::launch_decode(a, hp.ps >= 8 ? &map_rows : nullptr);
     if (e != cudaSuccess) return cuda_err(e, "decode launch");
   }
   if (stage_mask & PA_STAGE_MERGE) {

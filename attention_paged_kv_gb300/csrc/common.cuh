@@ -2,10 +2,10 @@
 // kernel parameters, and thin inline-PTX wrappers for the sm_103a features
 // the kernels use (mbarrier, TMA tensor copies, cp.async, tcgen05 / TMEM).
 //
-// Every wait on an mbarrier is bounded: after WAIT_LIMIT_CYCLES of polling,
-// or as soon as another thread of the CTA has given up, it returns false and
-// the kernel unwinds (see the kernels' abort paths).  Nothing here can spin
-// forever.
+// Every wait on an mbarrier is bounded: after the run's wait limit (about 2 s
+// of clock64 unless the plan set a shorter one), or as soon as another
+// thread of the CTA has given up, it returns false and the kernel unwinds
+// (see the kernels' abort paths).  Nothing here can spin forever.
 #pragma once
 
 #include <cstdint>
@@ -36,6 +36,7 @@ struct KParams {
   int32_t Hq, Hkv, D, ps, ps_shift, G, g_shift, causal, num_pages, n_items;
   int32_t hnd;              // cache layout: 0 NHD [P, 2, ps, Hkv, D], 1 HND [P, 2, Hkv, ps, D]
   float scale_log2;         // log2(e) / sqrt(D)
+  long long wait_limit;     // clock cycles a pipeline wait may poll before it gives up
 };
 
 // ---------------------------------------------------------------------------
@@ -54,6 +55,9 @@ __device__ __forceinline__ KvLoc kv_locate(const int32_t* pages, int32_t page_st
 // ---------------------------------------------------------------------------
 // small PTX wrappers
 
+// Default bound of a pipeline wait, and the bound of every drain wait (the
+// waits that let copies and MMAs in flight land before a CTA exits, which
+// never take the shorter limit a caller may set for the pipeline waits).
 #ifndef PA_WAIT_LIMIT_CYCLES
 #define PA_WAIT_LIMIT_CYCLES (4000000000LL)  // about 2 s at 2 GHz
 #endif
@@ -93,17 +97,17 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
 }
 
 // Bounded wait for the phase with the given parity to complete.  Returns
-// false (and records PA_DEV_TIMEOUT, and raises *abort_flag) when the limit
-// passes or when *abort_flag is already raised by another thread.
+// false (and records PA_DEV_TIMEOUT, and raises *abort_flag) when `limit`
+// clock cycles pass or when *abort_flag is already raised by another thread.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
-                                          int32_t* status) {
+                                          int32_t* status, long long limit) {
   const uint32_t a = smem_u32(bar);
   if (mbar_try_wait(a, parity)) return true;
   const long long t0 = clock64();
   while (true) {
     if (mbar_try_wait(a, parity)) return true;
     if (*abort_flag) return false;
-    if (clock64() - t0 > PA_WAIT_LIMIT_CYCLES) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       atomicOr(status, PA_DEV_TIMEOUT);
       return false;

@@ -96,7 +96,7 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
       const int st = j % kDecStages;
       if (j >= kDecStages) {
         bool ok = true;
-        if (lane == 0) ok = mbar_wait(&empty[st], ((j / kDecStages) - 1) & 1, abort_flag, p.status);
+        if (lane == 0) ok = mbar_wait(&empty[st], ((j / kDecStages) - 1) & 1, abort_flag, p.status, p.wait_limit);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
       }
@@ -228,7 +228,7 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode
     const int t0 = lane, t1 = lane + 32;
     for (int k = 0, j = pair; j < nstage; ++k, j += kDecPairs) {
       const int st = j % kDecStages;
-      bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status);
+      bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status, p.wait_limit);
       if (!__all_sync(0xffffffffu, ok)) break;
       const int nval = min(kDecTile, it.tok1 - (it.tok0 + j * kDecTile));
       const uint8_t* kst = smem + st * C::STAGE;
@@ -280,7 +280,7 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode
         m_run[g] = m_new;
       }
       if (k >= 1) {
-        ok = mbar_wait(&pempty[pair], (k - 1) & 1, abort_flag, p.status);
+        ok = mbar_wait(&pempty[pair], (k - 1) & 1, abort_flag, p.status, p.wait_limit);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
 #pragma unroll
@@ -314,8 +314,8 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode
       for (int i = 0; i < 4; ++i) o2[g][i] = make_float2(0.f, 0.f);
     for (int k = 0, j = pair; j < nstage; ++k, j += kDecPairs) {
       const int st = j % kDecStages;
-      bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status);
-      if (ok) ok = mbar_wait(&pfull[pair], k & 1, abort_flag, p.status);
+      bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status, p.wait_limit);
+      if (ok) ok = mbar_wait(&pfull[pair], k & 1, abort_flag, p.status, p.wait_limit);
       if (!__all_sync(0xffffffffu, ok)) break;
       const int nval = min(kDecTile, it.tok1 - (it.tok0 + j * kDecTile));
       const uint8_t* vst = smem + st * C::STAGE + C::STAGE_K;
@@ -565,7 +565,7 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
 
   for (int j = 0; j < nstage; ++j) {
     const int st = j % kDecStages;
-    const bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status);
+    const bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status, p.wait_limit);
     if (!__all_sync(0xffffffffu, ok)) break;
     const int s0 = it.tok0 + j * kDecTile;         // absolute position of the stage's first key
     const int nval = min(kDecTile, it.tok1 - s0);  // keys of the stage inside the item's range
@@ -818,12 +818,9 @@ __global__ void debug_gather_kernel(const KParams p, const int B, int32_t* page_
 template <typename T, int D, int G>
 cudaError_t launch_cuda_cores(const RunArgs& a, const CUtensorMap* map, const KParams& kp, int use_tma) {
   using C = DecCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<T, D, G>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_set{0};
+  cudaError_t e = set_smem_once(attr_set, reinterpret_cast<const void*>(decode_kernel<T, D, G>), C::SMEM);
+  if (e != cudaSuccess) return e;
   decode_kernel<T, D, G><<<a.hp->n_dec, kDecThreads, C::SMEM, a.stream>>>(*map, kp, use_tma);
   return cudaGetLastError();
 }
@@ -832,13 +829,9 @@ template <typename T, int D, int RC>
 cudaError_t launch_mma(const RunArgs& a, const CUtensorMap* map, const KParams& kp, int use_tma, int item0,
                        int n) {
   using C = DecCfg<D>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(decode_mma_kernel<T, D, RC>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_set{0};
+  cudaError_t e = set_smem_once(attr_set, reinterpret_cast<const void*>(decode_mma_kernel<T, D, RC>), C::SMEM);
+  if (e != cudaSuccess) return e;
   decode_mma_kernel<T, D, RC><<<n, kDmThreads, C::SMEM, a.stream>>>(*map, kp, use_tma, item0);
   return cudaGetLastError();
 }

@@ -1,8 +1,10 @@
 // Host-side internals shared by the planner, the C ABI and the launchers.
 #pragma once
 
+#include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -22,6 +24,7 @@ struct HostPlan {
   int32_t dec_cores = 0;                  // 1: decode items run on the CUDA-core kernel
   int32_t pre_tiles = 2;                  // 128-row Q tiles per prefill item (1 or 2)
   int32_t hnd = 0;                        // cache layout: 0 NHD, 1 HND
+  int32_t wait_limit_cycles = 0;          // > 0: bound of each pipeline wait (test hook)
   int32_t n_dec_class[4] = {0, 0, 0, 0};  // decode items per row class, consecutive in item order
   size_t blob_bytes = 0, off_part_o = 0, off_part_lse = 0, total_bytes = 0;
   size_t off_pages = 0, off_req = 0, off_dec = 0, off_pre = 0, off_merge = 0;
@@ -36,6 +39,7 @@ struct PlanInputs {
   int32_t B, Hq, Hkv, D, ps, num_pages, dtype, causal;
   int32_t num_sms, force_prefill, decode_chunk_pages, prefill_chunk_tiles, decode_cuda_cores, kv_layout;
   int32_t prefill_q_tiles;  // 0: the planner's choice, else 1 or 2 Q tiles per prefill item
+  int32_t wait_limit_cycles;  // > 0: bound of each pipeline wait in clock cycles (test hook)
   // shared-prefix cascade (n_groups == 0: a plain plan)
   const int32_t* group_indptr;
   const int32_t* prefix_page_indptr;
@@ -63,6 +67,20 @@ cudaError_t launch_decode(const RunArgs& a, const CUtensorMap* map_rows);
 cudaError_t launch_merge(const RunArgs& a);
 cudaError_t launch_debug_gather(const RunArgs& a, int32_t* page_out, int32_t* slot_out);
 
+// Raise `func`'s dynamic shared memory limit to `bytes` on the current
+// device, once per device: the attribute is per device, so `done` keeps one
+// bit per device ordinal.  Concurrent first calls may both set it (harmless).
+inline cudaError_t set_smem_once(std::atomic<uint64_t>& done, const void* func, int bytes) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+  if (bit && (done.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
+  return e;
+}
+
 // Error reporting into the thread-local last-error text (api.cu).
 pagedattn_status set_err(pagedattn_status s, const std::string& msg);
 pagedattn_status cuda_err(cudaError_t e, const char* what);
@@ -82,6 +100,8 @@ struct pagedattn_plan_s {
   size_t workspace_bytes = 0;
   int device = -1;
   int force_cp_async = 0;
+  // guards the tensor-map cache below: a plan may be run from several host threads
+  std::mutex maps_mu;
   // tensor maps over the last kv_cache pointer seen by run()
   const void* map_kv = nullptr;
   CUtensorMap map_rows;   // decode: box {64, 1, min(ps, 64), 1}, 128-byte swizzle (page_size >= 8)

@@ -17,7 +17,9 @@
 // capture.  Every call shares the array: its contents are whatever the last
 // call left, each call starts by copying the plan's metadata over it (which
 // also clears the status word), and calls that overlap on the GPU (on
-// different streams, or from different threads) race on it.
+// different streams, or from different threads) race on it.  The status word
+// the last call's kernels left there is read back by
+// pagedattn_noalloc_device_status.
 #include <cstring>
 #include <mutex>
 #include <string>
@@ -102,5 +104,25 @@ extern "C" pagedattn_status pagedattn_run_decode_noalloc(pagedattn_plan_t plan, 
   if (e != cudaSuccess) return cuda_err(e, "no-alloc decode launch");
   e = launch_merge(a);
   if (e != cudaSuccess) return cuda_err(e, "no-alloc merge launch");
+  return PA_OK;
+}
+
+extern "C" pagedattn_status pagedattn_noalloc_device_status(pagedattn_stream_t stream, int32_t* flags) {
+  using namespace pa;
+  if (!flags) return set_err(PA_ERR_INVALID_ARG, "flags is NULL");
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_err(e, "cudaGetDevice");
+  void* scratch = nullptr;
+  pagedattn_status s = scratch_address(dev, &scratch);
+  if (s != PA_OK) return s;
+  cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  e = cudaMemcpyAsync(&v, static_cast<int32_t*>(scratch) + H_STATUS, sizeof(v), cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_err(e, "no-alloc status read");
+  *flags = v;
+  if (v & PA_DEV_TIMEOUT) return set_err(PA_ERR_TIMEOUT, "an in-kernel wait gave up after its bound");
+  if (v) return set_err(PA_ERR_DEVICE_CHECK, "an in-kernel check fired (flags " + std::to_string(v) + ")");
   return PA_OK;
 }

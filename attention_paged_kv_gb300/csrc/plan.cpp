@@ -436,6 +436,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   hp->dec_cores = dec_cores;
   hp->pre_tiles = pre_tiles;
   hp->hnd = in.kv_layout;
+  hp->wait_limit_cycles = in.wait_limit_cycles;
   for (int c = 0; c < kDecClasses; ++c) hp->n_dec_class[c] = n_class[c];
   hp->blob_bytes = size_t(blob_bytes); hp->off_part_o = size_t(off_part_o);
   hp->off_part_lse = size_t(off_part_lse); hp->total_bytes = size_t(total);

@@ -98,8 +98,8 @@ __device__ __forceinline__ float ex2(float x) {
 
 // Bounded wait, made uniform across the warp (all lanes leave together).
 __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
-                                          int32_t* status) {
-  bool ok = mbar_wait(bar, parity, abort_flag, status);
+                                          int32_t* status, long long limit) {
+  bool ok = mbar_wait(bar, parity, abort_flag, status, limit);
   return __all_sync(0xffffffffu, ok);
 }
 
@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
         uint64_t* full = half ? full_v : full_k;
         const uint32_t dst0 = half ? v_addr(st) : k_addr(st);
         if (j >= NST) {
-          if (lane == 0) ok = mbar_wait(&empty[st], ((j / NST) - 1) & 1, abort_flag, p.status);
+          if (lane == 0) ok = mbar_wait(&empty[st], ((j / NST) - 1) & 1, abort_flag, p.status, p.wait_limit);
           ok = __shfl_sync(0xffffffffu, ok, 0);
           if (!ok) break;
         }
@@ -309,8 +309,8 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       // tile A's P_lo of the first key tile may live in K slot 0: then that
       // slot is released only once PV_A(0) has read it
       const bool plo_in_k = lo_split0 && (C::OFF_PLO_A == C::OFF_K);
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status);
-      if (ok) ok = mbar_wait(&full_k[0], 0, abort_flag, p.status);
+      bool ok = mbar_wait(q_full, 0, abort_flag, p.status, p.wait_limit);
+      if (ok) ok = mbar_wait(&full_k[0], 0, abort_flag, p.status, p.wait_limit);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
@@ -321,21 +321,21 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
         const int st = j % NST;
         const bool more = j + 1 < nkt;
         const int st1 = (j + 1) % NST;
-        ok = mbar_wait(&p_full[0], j & 1, abort_flag, p.status);
-        if (ok) ok = mbar_wait(&full_v[st], (j / NST) & 1, abort_flag, p.status);
+        ok = mbar_wait(&p_full[0], j & 1, abort_flag, p.status, p.wait_limit);
+        if (ok) ok = mbar_wait(&full_v[st], (j / NST) & 1, abort_flag, p.status, p.wait_limit);
         if (!ok) break;
         tc_fence_after();
         issue_pv(0, j, st);
         if (j == 0 && plo_in_k) tc_commit(&empty_k[0]);
         if (more) {
-          ok = mbar_wait(&full_k[st1], ((j + 1) / NST) & 1, abort_flag, p.status);
+          ok = mbar_wait(&full_k[st1], ((j + 1) / NST) & 1, abort_flag, p.status, p.wait_limit);
           if (!ok) break;
           tc_fence_after();
           issue_s(0, st1);
           if (!has_b) tc_commit(&empty_k[st1]);
         }
         if (has_b) {
-          ok = mbar_wait(&p_full[1], j & 1, abort_flag, p.status);
+          ok = mbar_wait(&p_full[1], j & 1, abort_flag, p.status, p.wait_limit);
           if (!ok) break;
           tc_fence_after();
           issue_pv(1, j, st);
@@ -371,7 +371,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
 
     for (int j = 0; ok && j < nkt; ++j) {
       const int k0 = it.kv_tok0 + j * kKvTile;
-      ok = warp_wait(&s_full[x], j & 1, abort_flag, p.status);
+      ok = warp_wait(&s_full[x], j & 1, abort_flag, p.status, p.wait_limit);
       if (!ok) break;
       tc_fence_after();
       const int lim = row_end - k0;
@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       const bool lo_split = lo_split0 && j == 0;
       if (lo_split && x == 0 && C::OFF_PLO_A == C::OFF_K && has_b) {
         // tile A's P_lo reuses K stage 0: S_B(0) must be done reading it
-        ok = warp_wait(&s_full[1], 0, abort_flag, p.status);
+        ok = warp_wait(&s_full[1], 0, abort_flag, p.status, p.wait_limit);
         if (!ok) break;
       }
 
@@ -466,7 +466,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       // S_x(j) done implies PV_x(j-1) done (the MMAs run in issue order); the
       // barrier makes O's contents visible before it is rescaled
       if (j >= 1) {
-        ok = warp_wait(&o_done[x], (j - 1) & 1, abort_flag, p.status);
+        ok = warp_wait(&o_done[x], (j - 1) & 1, abort_flag, p.status, p.wait_limit);
         if (!ok) break;
         tc_fence_after();
       }
@@ -487,7 +487,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
         const int valid = it.kv_tok1 - k0;
         if (valid < kKvTile) {
           const int st = j % NST;
-          ok = warp_wait(&full_v[st], (j / NST) & 1, abort_flag, p.status);
+          ok = warp_wait(&full_v[st], (j / NST) & 1, abort_flag, p.status, p.wait_limit);
           if (!ok) break;
           if (r >= valid) {
             uint8_t* vrow = smem + C::OFF_V + st * C::KV_BYTES + r * 128;
@@ -508,7 +508,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     }
 
     // ---------------------------------------------------------------- epilogue
-    if (ok && (x == 0 || has_b)) ok = warp_wait(&o_done[x], (nkt - 1) & 1, abort_flag, p.status);
+    if (ok && (x == 0 || has_b)) ok = warp_wait(&o_done[x], (nkt - 1) & 1, abort_flag, p.status, p.wait_limit);
     if (ok && (x == 0 || has_b)) {
       tc_fence_after();
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
@@ -553,6 +553,9 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
   }
 
   // ---------------------------------------------------------------- teardown
+  // a softmax warp that gave up between its P stores and their wait still
+  // has TMEM stores in flight: they complete before TMEM is released
+  if (warp < C::WARP_PROD) tmem_wait_st();
   tc_fence_before();
   __syncthreads();
   if (warp == C::WARP_MMA) {
@@ -565,13 +568,9 @@ template <typename T, int D, int NT>
 cudaError_t launch_prefill_t(const RunArgs& a, const CUtensorMap* kv_map, const CUtensorMap* q_map,
                              const KParams& kp, int use_tma) {
   using C = PreCfg<D, NT>;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e =
-        cudaFuncSetAttribute(prefill_kernel<T, D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  static std::atomic<uint64_t> attr_set{0};
+  cudaError_t e = set_smem_once(attr_set, reinterpret_cast<const void*>(prefill_kernel<T, D, NT>), C::SMEM);
+  if (e != cudaSuccess) return e;
   prefill_kernel<T, D, NT><<<a.hp->n_pre, C::THREADS, C::SMEM, a.stream>>>(*kv_map, *q_map, kp, use_tma);
   return cudaGetLastError();
 }

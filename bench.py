@@ -30,6 +30,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -47,6 +48,10 @@ WORKLOADS = {
     "prefix_decode": lambda wl: wl.prefix_decode(),
     "prefix_decode_cascade": lambda wl: wl.prefix_decode(),
     "specdec": lambda wl: wl.mixed(prefill_len=0, decode_qo=4),
+    # profiling captures of one kernel each, a GB or less on the device
+    "decode_g2": lambda wl: wl.decode(batch_size=512, num_qo_heads=2),
+    "decode_mixed64": lambda wl: wl.mixed(prefill_len=0, num_decode=64),
+    "specdec8": lambda wl: wl.mixed(prefill_len=0, num_decode=64, decode_qo=8),
 }
 # workloads planned as a shared-prefix cascade: (group_indptr, prefix pages per group)
 CASCADE = {"prefix_cascade": ([0, 64], [12]), "prefix_decode_cascade": ([0, 64], [256])}
@@ -156,6 +161,82 @@ def graph_ms(plan, bufs, stages, reps):
     return e0.elapsed_time(e1) / (reps * len(bufs))
 
 
+def time_workload(pa, w, dev, steps, popts=None, pargs=None):
+    """Device time of one step of a small batch and of each of its stages:
+    a CUDA graph over enough copies of q, out and the cache that no step
+    finds the previous one's data in L2 (graph_ms).  Returns a dict."""
+    import torch
+    popts = dict(popts or {})
+    pargs = pargs or w.plan_args()
+    plan = pa.Plan(**pargs, dtype=w.dtype, **popts)
+    hdr = plan.dump()[:32]
+    n_dec, n_pre, n_merge = int(hdr[12]), int(hdr[13]), int(hdr[14])
+    q, kv = w.q.to(dev), w.kv_cache.to(dev)
+    n_rot = rotation_count(w)
+    bufs = [(q, kv, torch.empty_like(q), torch.empty(q.shape[0], q.shape[1], dtype=torch.float32, device=dev))]
+    bufs += [(q.clone(), kv.clone(), torch.empty_like(q), torch.empty_like(bufs[0][3])) for _ in range(n_rot - 1)]
+    sh = torch.cuda.current_stream(dev).cuda_stream
+    for _ in range(3):
+        for q_, kv_, o_, l_ in bufs:
+            plan.run_ptrs(q_.data_ptr(), kv_.data_ptr(), o_.data_ptr(), l_.data_ptr(), sh)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0, pa.last_error()
+    reps = max(1, -(-steps // n_rot))
+    res = {"step_ms": graph_ms(plan, bufs, pa.PA_STAGE_ALL, reps),
+           "prefill_ms": graph_ms(plan, bufs, pa.PA_STAGE_PREFILL, reps) if n_pre else 0.0,
+           "decode_ms": graph_ms(plan, bufs, pa.PA_STAGE_DECODE, reps) if n_dec else 0.0,
+           "merge_ms": graph_ms(plan, bufs, pa.PA_STAGE_MERGE, reps) if n_merge else 0.0,
+           "items": {"prefill": n_pre, "decode": n_dec, "merge": n_merge}, "copies": n_rot,
+           "decode_kernel": "decode_kernel" if int(hdr[29]) else "decode_mma_kernel"}
+    assert plan.device_status() == 0, pa.last_error()
+    plan.close()
+    return res
+
+
+def config_records(pa, workloads, dev, peaks, steps):
+    """The other workloads of the pages next to the benchmark step, each
+    timed on its own (time_workload): the decode timing script's batch
+    (decode against HBM), the ragged short prompts against the same batch
+    padded to 200 tokens, and the shared-prefix batch against its
+    duplicated-pages twin and its shared-prefix cascade plan."""
+    bw = peaks["hbm_gbs"] * 1e9
+    ptc = peaks["bf16_tflops"] * 1e12
+
+    def roof_frac(acc, ms):
+        return max(acc["flops"] / ptc, acc["bytes"] / bw) / (ms * 1e-3)
+
+    rec = {}
+    w = workloads.decode()
+    acc = accounting(w)
+    t = time_workload(pa, w, dev, steps)
+    dec_ms = t["decode_ms"] + t["merge_ms"]
+    rec["decode_script"] = {
+        "workload": WORKLOAD_DESC["decode"], "step_us": t["step_ms"] * 1e3, "decode_us": t["decode_ms"] * 1e3,
+        "merge_us": t["merge_ms"] * 1e3, "kernel": t["decode_kernel"] + ("+merge_kernel" if t["merge_ms"] else ""),
+        "kv_gbs": acc["decode"]["kv_bytes"] / (dec_ms * 1e-3) / 1e9,
+        "all_bytes_gbs": acc["decode"]["bytes"] / (dec_ms * 1e-3) / 1e9,
+        "frac_of_hbm": acc["decode"]["bytes"] / (dec_ms * 1e-3) / bw,
+        "step_frac_of_hbm": acc["bytes"] / (t["step_ms"] * 1e-3) / bw, "bytes": acc["bytes"],
+        "items": t["items"], "l2": f"{t['copies']} copies of q, out and the cache cycled by a CUDA graph"}
+    del w
+    a, b = workloads.ragged(), workloads.ragged(padded=True)
+    ta, tb = time_workload(pa, a, dev, steps), time_workload(pa, b, dev, steps)
+    acc = accounting(a)
+    rec["ragged"] = {"workload": WORKLOAD_DESC["ragged"], "step_us": ta["step_ms"] * 1e3,
+                     "padded_step_us": tb["step_ms"] * 1e3, "padded_over_unpadded": tb["step_ms"] / ta["step_ms"],
+                     "frac_of_roofline": roof_frac(acc, ta["step_ms"]),
+                     "tflops": acc["flops"] / (ta["step_ms"] * 1e-3) / 1e12, "items": ta["items"]}
+    a, b = workloads.prefix(), workloads.prefix(duplicated=True)
+    ta, tb = time_workload(pa, a, dev, steps), time_workload(pa, b, dev, steps)
+    groups, pargs = workloads.split_prefix(a, *CASCADE["prefix_cascade"])
+    tc = time_workload(pa, a, dev, steps, popts={"prefix_groups": groups}, pargs=pargs)
+    acc = accounting(a)
+    rec["prefix"] = {"workload": WORKLOAD_DESC["prefix"], "step_us": ta["step_ms"] * 1e3,
+                     "duplicated_step_us": tb["step_ms"] * 1e3, "cascade_step_us": tc["step_ms"] * 1e3,
+                     "frac_of_roofline": roof_frac(acc, ta["step_ms"]), "items": ta["items"]}
+    return rec
+
+
 def load_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
@@ -202,17 +283,26 @@ class ClockSampler:
     def __init__(self, device_index: int):
         self.dev = device_index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{device_index}.csv")
+        fd, self.path = tempfile.mkstemp(prefix=f"pagedattn_clocks_{device_index}_", suffix=".csv")
+        os.close(fd)
 
-    def start(self):
+    def start(self, first_sample_timeout: float = 3.0):
+        """Start sampling every 100 ms; returns once the first sample is in
+        (or after ``first_sample_timeout`` seconds), so that the region that
+        follows is covered from its start."""
         try:
-            os.makedirs(os.path.dirname(self.path), exist_ok=True)
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
+            return
+        t0 = time.time()
+        while time.time() - t0 < first_sample_timeout:
+            if os.path.getsize(self.path) > 0:
+                break
+            time.sleep(0.02)
 
     def stop(self):
         if self.proc is None:
@@ -224,8 +314,13 @@ class ClockSampler:
             self.proc.kill()
         self.f.close()
         sm, mx, reasons = [], None, set()
+        lines = open(self.path).read().splitlines()
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
+        for line in lines:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) < 9:
                 continue
@@ -271,17 +366,48 @@ def oracle_sample(w, n_tok: int, n_dec: int):
     return elapsed, flops, desc
 
 
-def calibrate_sample(w, seconds: float):
-    """Smallest doubling of (prefill tokens, decode requests) whose oracle
-    time reaches ``seconds`` (or the largest tried)."""
-    n_tok, n_dec = 1, 1
-    n_dec_max = int((np.diff(w.qo_indptr) == 1).sum())
-    while True:
+# The one sample both oracle legs time (the cpu_baseline of our arm and every
+# step of the reference arm): this many prefill query tokens spread over the
+# prompt and this many decode requests, all query heads.
+ORACLE_SAMPLE = (16, 16)
+
+
+def oracle_step_seconds(w, acc, reps: int):
+    """Median over ``reps`` runs of the fixed oracle sample, scaled to the
+    whole step by algorithmic flops.  Returns (step seconds, list of the
+    per-run sample seconds, description)."""
+    n_tok, n_dec = ORACLE_SAMPLE
+    runs, fl, desc = [], 0, ""
+    for _ in range(reps):
         el, fl, desc = oracle_sample(w, n_tok, n_dec)
-        if el >= seconds or n_tok >= 1024:
-            return n_tok, n_dec, el, fl, desc
-        grow = max(2, min(8, int(seconds / max(el, 1e-3))))
-        n_tok, n_dec = n_tok * grow, min(n_dec * grow, n_dec_max)
+        runs.append(el)
+    return statistics.median(runs) * acc["flops"] / fl, runs, desc
+
+
+def blas_threads():
+    """Threads of the BLAS that numpy (the oracle's matmuls) calls: from
+    threadpoolctl when installed, else from OpenBLAS's own query function in
+    the loaded library, else None."""
+    try:
+        import threadpoolctl
+        info = [d for d in threadpoolctl.threadpool_info() if d.get("user_api") == "blas"]
+        if info:
+            return int(info[0]["num_threads"])
+    except Exception:
+        pass
+    try:
+        import ctypes
+        for line in open("/proc/self/maps"):
+            path = line.split()[-1]
+            if "openblas" in os.path.basename(path) and path.endswith(".so") or ".so." in path and "openblas" in path:
+                lib = ctypes.CDLL(path)
+                for fn in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_",
+                           "openblas_get_num_threads"):
+                    if hasattr(lib, fn):
+                        return int(getattr(lib, fn)())
+    except Exception:
+        pass
+    return None
 
 
 def cpu_cores():
@@ -297,12 +423,13 @@ def cpu_cores():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the decode / ragged / prefix sub-records")
     ap.add_argument("--decode-chunk-pages", type=int, default=0, help="planner override (0: the plan's rule)")
     ap.add_argument("--prefill-chunk-tiles", type=int, default=0, help="planner override (0: the plan's rule)")
     ap.add_argument("--prefill-q-tiles", type=int, default=0, help="planner override (0: the plan's rule)")
@@ -325,23 +452,17 @@ def main():
         acc = accounting(w)
         peaks, peak_src = load_peaks()
         roof_t = max(acc["flops"] / (peaks["bf16_tflops_sustained"] * 1e12), acc["bytes"] / (peaks["hbm_gbs"] * 1e9))
-        # each step: one bounded oracle sample, sized so that W + K steps take ~2 minutes
-        per_step = max(0.05, 120.0 / (args.warmup + args.steps))
-        n_tok, n_dec, _, _, desc = calibrate_sample(w, per_step)
-        times = []
-        for i in range(args.warmup + args.steps):
-            el, fl, desc = oracle_sample(w, n_tok, n_dec)
-            if i >= args.warmup:
-                times.append(el * acc["flops"] / fl)
-        step_t = statistics.median(times)
+        # every step: the fixed oracle sample, scaled to the whole step by flops
+        oracle_step_seconds(w, acc, args.warmup)
+        step_t, runs, desc = oracle_step_seconds(w, acc, args.steps)
         val = 100.0 * roof_t / step_t
         line = {"impl": "reference", "metric": METRIC, "value": val, "unit": UNIT, "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_t * 1e3, "higher_is_better": True,
                 "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-                "config": {"workload": "mixed", "note": "each timed step is a bounded sample of the step, "
-                           "scaled to the whole step by algorithmic flops"},
-                "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-                                 "sample": desc},
+                "config": {"workload": "mixed", "note": "each timed step is the fixed oracle sample of the step, "
+                           "scaled to the whole step by algorithmic flops (median over the steps)"},
+                "cpu_baseline": {"value": val, "unit": UNIT, "cores": cpu_cores(), "blas_threads": blas_threads(),
+                                 "kind": "oracle", "sample": desc, "sample_seconds": statistics.median(runs)},
                 "e2e": {"value": val, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -402,10 +523,10 @@ def main():
         torch.cuda.synchronize()
         clk.start()
         total_ms = graph_ms(plan, bufs, pa.PA_STAGE_ALL, reps) * K
-        clocks = clk.stop()
         t_pre = graph_ms(plan, bufs, pa.PA_STAGE_PREFILL, reps) if n_pre else 0.0
         t_dec = graph_ms(plan, bufs, pa.PA_STAGE_DECODE, reps) if n_dec else 0.0
         t_mrg = graph_ms(plan, bufs, pa.PA_STAGE_MERGE, reps) if n_merge else 0.0
+        clocks = clk.stop()
         if world > 1:
             torch.distributed.barrier()
     else:
@@ -422,7 +543,6 @@ def main():
             plan.run_ptrs(qp, kvp, op, lp, sh, pa.PA_STAGE_ALL)
         t_end.record(stream)
         torch.cuda.synchronize()
-        clocks = clk.stop()
         if world > 1:
             torch.distributed.barrier()
         total_ms = t_start.elapsed_time(t_end)
@@ -439,6 +559,7 @@ def main():
             plan.run_ptrs(qp, kvp, op, lp, sh, pa.PA_STAGE_MERGE)
             e[3].record(stream)
         torch.cuda.synchronize()
+        clocks = clk.stop()  # sampled over both timed loops
         # a stage with no items launches nothing: its event pair only measures the gap
         t_pre = sum(e[0].elapsed_time(e[1]) for e in ev) / K if n_pre else 0.0
         t_dec = sum(e[1].elapsed_time(e[2]) for e in ev) / K if n_dec else 0.0
@@ -461,8 +582,7 @@ def main():
     prefill_obj = {"kernel": "prefill_kernel", "ms": t_pre, "tflops": pre_tflops,
                    "frac_of_bf16_peak": pre_tflops / p_tc, "flops": acc["prefill"]["flops"],
                    "bytes": acc["prefill"]["bytes"]}
-    G = w.num_qo_heads // w.num_kv_heads
-    dec_name = "decode_mma_kernel" if G in (4, 8) else "decode_kernel"
+    dec_name = "decode_kernel" if int(hdr[29]) else "decode_mma_kernel"  # the plan's choice
     decode_obj = {"kernel": f"{dec_name}+merge_kernel", "ms": dec_time, "decode_ms": t_dec, "merge_ms": t_mrg,
                   "kv_gbs": dec_gbs, "all_bytes_gbs": dec_all_gbs, "frac_of_hbm": dec_all_gbs / peaks["hbm_gbs"],
                   "kv_bytes": acc["decode"]["kv_bytes"], "bytes": acc["decode"]["bytes"]}
@@ -484,10 +604,15 @@ def main():
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        n_tok, n_dec, el, fl, desc = calibrate_sample(w, 12.0)
-        cpu_step = el * acc["flops"] / fl
-        cpu = {"value": 100.0 * roof_t / cpu_step, "unit": UNIT, "cores": cpu_cores(), "kind": "oracle",
-               "sample": desc, "sample_seconds": el, "ms_per_step_extrapolated": cpu_step * 1e3}
+        cpu_step, runs, desc = oracle_step_seconds(w, acc, 5)
+        cpu = {"value": 100.0 * roof_t / cpu_step, "unit": UNIT, "cores": cpu_cores(),
+               "blas_threads": blas_threads(), "kind": "oracle",
+               "sample": desc + " (median of 5 runs)", "sample_seconds": statistics.median(runs),
+               "ms_per_step_extrapolated": cpu_step * 1e3}
+
+    configs = None
+    if rank == 0 and not args.no_configs and args.workload == "mixed":
+        configs = config_records(pa, workloads, dev, peaks, 200)
 
     if rank == 0:
         line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": K, "warmup": args.warmup,
@@ -501,7 +626,7 @@ def main():
                                   f"a CUDA graph of one step per copy"),
                            "roofline_time_ms": roof_t * 1e3, "plan_ms": t_plan * 1e3,
                            "items": {"prefill": n_pre, "decode": n_dec, "merge": n_merge}},
-                "roofline": roof, "prefill": prefill_obj, "decode": decode_obj,
+                "roofline": roof, "prefill": prefill_obj, "decode": decode_obj, "configs": configs,
                 "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": launches_per_step * K, "clocks": clocks}
         print(json.dumps(line), flush=True)
     if world > 1:
@@ -524,6 +649,11 @@ WORKLOAD_DESC = {
     "prefix_decode_cascade": "the same 64 decodes planned as a shared-prefix cascade",
     "specdec": "speculative decoding: 256 requests x 4 query tokens, kv_len U[512,8192]; Hq 64 / Hkv 8, "
                "head_dim 128, page_size 16, bf16",
+    "decode_g2": "the decode script's shape re-headed to Hq 2 / Hkv 1 (CUDA-core decode kernel), 512 requests "
+                 "x 1024 keys, fp16",
+    "decode_mixed64": "64 decodes with kv_len U[512,8192], Hq 64 / Hkv 8, head_dim 128, page_size 16, bf16",
+    "specdec8": "64 requests x 8 query tokens (64 packed rows a kv head), kv_len U[512,8192], Hq 64 / Hkv 8, "
+                "head_dim 128, page_size 16, bf16",
 }
 
 

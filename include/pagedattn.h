@@ -89,6 +89,11 @@ typedef struct {
   int32_t prefill_q_tiles;     /* 128-row query tiles per prefill work item: 1 or 2;
                                   0 = the planner's choice (see plan).  head_dim 256
                                   takes 1 only                                      */
+  int32_t wait_limit_cycles;   /* test hook: > 0 bounds every in-kernel pipeline wait
+                                  at that many SM clock cycles instead of about 2 s,
+                                  so a test can make the waits give up (the run then
+                                  reports PA_DEV_TIMEOUT through device_status and
+                                  leaves out / lse undefined); 0 = the default      */
   int32_t reserved[1];         /* must be 0                                          */
 } pagedattn_options;
 
@@ -239,7 +244,10 @@ PAGEDATTN_API pagedattn_status pagedattn_workspace_size_cascade(const pagedattn_
  * split, the merge kernel, in that order on `stream`.  Allocates nothing and does not synchronise the host.  In-kernel
  * waits are bounded; a wait that gives up sets PA_DEV_TIMEOUT in the device
  * status word (read it with pagedattn_device_status).  Calls that overlap on
- * the device must use different workspaces (the partial states live there).
+ * the device must use different workspaces (the partial states live there),
+ * so two such calls need two plans.  Host threads may call run on one plan
+ * at once: the plan's host-side state (its cache of TMA descriptors) is
+ * locked; kernel launch settings are applied per device.
  */
 PAGEDATTN_API pagedattn_status pagedattn_run(pagedattn_plan_t plan, const void* q, const void* kv_cache,
                                void* out, float* lse, pagedattn_stream_t stream);
@@ -311,12 +319,22 @@ PAGEDATTN_API pagedattn_status pagedattn_debug_gather(pagedattn_plan_t plan, int
  * Every call overwrites the array, whose contents are whatever the last call
  * left (the plan's metadata copy clears the in-kernel status word): calls
  * that overlap on the GPU -- on different streams or from different host
- * threads -- race and must not be issued.  The in-kernel status word of this
- * variant is not reported.
+ * threads -- race and must not be issued.  The in-kernel status word of the
+ * last call is read with pagedattn_noalloc_device_status.
  */
 PAGEDATTN_API pagedattn_status pagedattn_run_decode_noalloc(pagedattn_plan_t plan, const void* q,
                                                             const void* kv_cache, void* out, float* lse,
                                                             pagedattn_stream_t stream);
+
+/*
+ * The device status word (PA_DEV_* bits) that the kernels of the last
+ * pagedattn_run_decode_noalloc call on the current device left in the
+ * library's no-alloc array: waits for `stream` (pass the stream of that
+ * call), copies the word into *flags and returns PA_ERR_TIMEOUT /
+ * PA_ERR_DEVICE_CHECK when a bit is set, PA_OK otherwise.  Allocates
+ * nothing; the next no-alloc call clears the word.
+ */
+PAGEDATTN_API pagedattn_status pagedattn_noalloc_device_status(pagedattn_stream_t stream, int32_t* flags);
 
 /* Library version as "major.minor.patch". */
 PAGEDATTN_API const char* pagedattn_version(void);

@@ -239,6 +239,14 @@ def attention(w, form: str = "gather", **kw):
 # sampled rows (for batches too large to run whole on the CPU)
 
 
+def request_of_row(qo_indptr, row: int) -> int:
+    """The request b whose query rows [qo_indptr[b], qo_indptr[b+1]) hold the
+    packed row ``row`` (the CSR query layout of the timing script's
+    ``qo_indptr``).  A request with qo_len 0 owns no row, so the answer is
+    the last b with qo_indptr[b] <= row."""
+    return int(np.searchsorted(np.asarray(qo_indptr), row, side="right") - 1)
+
+
 def attention_rows(w, rows: Iterable[Tuple[int, int]], sm_scale=None) -> Dict[Tuple[int, int], Tuple[np.ndarray, float]]:
     """fp64 (out[D], lse) for the given (packed query row, query head) pairs.
     Rows of one (request, kv head) share one gather."""
@@ -249,7 +257,7 @@ def attention_rows(w, rows: Iterable[Tuple[int, int]], sm_scale=None) -> Dict[Tu
     indices = np.asarray(w.kv_page_indices, np.int64)
     by_group: Dict[Tuple[int, int], List[Tuple[int, int]]] = {}
     for (row, h) in rows:
-        b = int(np.searchsorted(qo_indptr, row, side="right") - 1)
+        b = request_of_row(qo_indptr, row)
         by_group.setdefault((b, kv_head_of(h, group)), []).append((row, h))
     res = {}
     for (b, g), items in by_group.items():

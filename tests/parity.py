@@ -6,16 +6,24 @@ import attention_paged_kv_gb300 as pa
 
 LSE_TOL = 1e-3
 
+# R7 allowance bookkeeping: bf16 outputs admitted only by the half-ulp term,
+# out of all bf16 outputs compared (reported at the end of the session)
+ALLOWANCE = {"used": 0, "compared": 0}
+
 
 def out_tol(ref: np.ndarray, dtype) -> np.ndarray:
-    """Per-element bound: 2e-3 (fp16) / 1e-2 (bf16), or half an ulp of the
-    output dtype at |ref| plus 1e-3 where that is larger (a bf16 value in
-    [4, 8) already has a half-ulp of 0.0156)."""
-    base = 2e-3 if dtype == torch.float16 else 1e-2
-    mant = 10 if dtype == torch.float16 else 7
+    """Per-element bound on |out - oracle|: 2e-3 flat for fp16; for bf16
+    1e-2, or half an ulp of bf16 at |ref| plus 1e-3 where that is larger (a
+    bf16 value in [4, 8) already has a half-ulp of 0.0156, so a correctly
+    rounded output can sit above 1e-2 from the exact value).  fp16 needs no
+    such allowance: its half-ulp stays below 2e-3 up to |ref| = 4, and these
+    N(0, 1) inputs give outputs of magnitude < 4."""
+    ref = np.asarray(ref)
+    if dtype == torch.float16:
+        return np.full(ref.shape, 2e-3)
     a = np.maximum(np.abs(ref), 2.0 ** -14)
-    half_ulp = 0.5 * 2.0 ** (np.floor(np.log2(a)) - mant)
-    return np.maximum(base, half_ulp + 1e-3)
+    half_ulp = 0.5 * 2.0 ** (np.floor(np.log2(a)) - 7)
+    return np.maximum(1e-2, half_ulp + 1e-3)
 
 
 def run(w, q=None, kv=None, **opts):
@@ -31,16 +39,24 @@ def run(w, q=None, kv=None, **opts):
 
 
 def assert_close(out, lse, ref_out, ref_lse, dtype, rows=None, what=""):
-    """Element-wise check of out (tolerance above) and lse (1e-3)."""
+    """Element-wise check of out (tolerance above) and lse (1e-3).  Returns
+    (max out error, max lse error, outputs admitted only by the bf16 half-ulp
+    allowance); the last is 0 for fp16 by construction."""
     if rows is not None:
         out, lse, ref_out, ref_lse = out[rows], lse[rows], ref_out[rows], ref_lse[rows]
     assert np.isfinite(out).all(), f"{what}: non-finite output"
     err = np.abs(out - ref_out)
     tol = out_tol(ref_out, dtype)
     bad = err > tol
-    allowance = int(((err > (2e-3 if dtype == torch.float16 else 1e-2)) & ~bad).sum())
+    flat = 2e-3 if dtype == torch.float16 else 1e-2
+    allowance = int(((err > flat) & ~bad).sum())
     assert not bad.any(), (f"{what}: {int(bad.sum())} outputs off, max err {err.max():.3e} "
                            f"at {np.unravel_index(err.argmax(), err.shape)}")
+    if dtype == torch.float16:
+        assert allowance == 0
+    else:
+        ALLOWANCE["used"] += allowance
+        ALLOWANCE["compared"] += int(err.size)
     lerr = np.abs(lse - ref_lse)
     assert (lerr <= LSE_TOL).all(), f"{what}: lse max err {lerr.max():.3e}"
     return float(err.max()), float(lerr.max()), allowance

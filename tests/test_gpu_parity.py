@@ -455,3 +455,104 @@ def test_cascade_shared_prefix_decode(cuda_cores):
     assert h["n_groups"] == 1 and h["n_pre"] > 0 and h["n_dec"] > 0
     ro, rl = A.attention(w)
     assert_close(out, lse, ro, rl, w.dtype, what="cascade decode")
+
+
+# ---------------------------------------------------------------- failure handling and host threads
+
+
+@pytest.mark.parametrize("name,opts", [
+    ("tiny", {}), ("tiny", {"force_prefill": True}), ("tiny", {"force_prefill": True, "prefill_q_tiles": 1}),
+    ("tiny", {"force_cp_async": True, "force_prefill": True}),
+    ("decode", {"decode_chunk_pages": 4}), ("decode", {"decode_cuda_cores": True, "decode_chunk_pages": 4})])
+def test_wait_limit_gives_up_then_normal_run(name, opts):
+    """Every in-kernel pipeline wait is bounded.  With the bound cut to one
+    clock cycle (the wait_limit_cycles test hook) the first wait that finds
+    its data not yet there gives up: the CTA drains the copies and MMAs it
+    has in flight, releases its TMEM and returns, and the run reports
+    PA_DEV_TIMEOUT through the device status word.  A normal run on the same
+    workspace afterwards matches the oracle."""
+    w = workloads.tiny() if name == "tiny" else workloads.decode(batch_size=16, seq_len=1000)
+    ws = torch.empty(pa.DEFAULT_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
+    q, kv = w.q.cuda(), w.kv_cache.cuda()
+    plan = pa.Plan(**w.plan_args(), dtype=w.dtype, workspace=ws, wait_limit_cycles=1, **opts)
+    plan.run(q, kv)
+    torch.cuda.synchronize()
+    flags = plan.device_status()
+    assert flags & pa.PA_DEV_TIMEOUT, f"no wait gave up (flags {flags})"
+    plan.close()
+    ro, rl = A.attention(w)
+    plan = pa.Plan(**w.plan_args(), dtype=w.dtype, workspace=ws, **opts)
+    out, lse = plan.run(q, kv)
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0, pa.last_error()
+    assert_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, w.dtype,
+                 what=f"after a timed-out run {opts}")
+
+
+def test_host_threads():
+    """Host threads: (a) two threads, each with its own plan, workspace and
+    stream, run at the same time; (b) two threads run one plan on one shared
+    stream, each alternating between two copies of the cache, so that the
+    plan's cached TMA descriptors are re-made on almost every call.  Every
+    result matches the oracle."""
+    import threading
+    wa = workloads.mixed(num_decode=24, prefill_len=700, kv_lo=16, kv_hi=3000)
+    wb = workloads.ragged()
+    refs = {id(w): A.attention(w) for w in (wa, wb)}
+    errors = []
+
+    def own_plan(w, reps):
+        try:
+            st = torch.cuda.Stream()
+            q, kv = w.q.cuda(), w.kv_cache.cuda()
+            torch.cuda.synchronize()
+            plan = pa.Plan(**w.plan_args(), dtype=w.dtype, stream=st)
+            outs = []
+            for _ in range(reps):
+                outs.append(plan.run(q, kv, stream=st))
+            st.synchronize()
+            assert plan.device_status(stream=st) == 0
+            ro, rl = refs[id(w)]
+            for out, lse in outs:
+                assert_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, w.dtype,
+                             what="own plan, own thread")
+        except Exception as e:  # reported by the main thread
+            errors.append(e)
+
+    ts = [threading.Thread(target=own_plan, args=(w, 6)) for w in (wa, wb)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    assert not errors, errors
+
+    w = wa
+    st = torch.cuda.Stream()
+    q = w.q.cuda()
+    kvs = [w.kv_cache.cuda(), w.kv_cache.cuda()]
+    torch.cuda.synchronize()
+    plan = pa.Plan(**w.plan_args(), dtype=w.dtype, stream=st)
+    results = {0: [], 1: []}
+
+    def shared_plan(k):
+        try:
+            for i in range(8):
+                results[k].append(plan.run(q, kvs[(i + k) % 2], stream=st))
+        except Exception as e:
+            errors.append(e)
+
+    ts = [threading.Thread(target=shared_plan, args=(k,)) for k in (0, 1)]
+    for t in ts:
+        t.start()
+    for t in ts:
+        t.join()
+    st.synchronize()
+    assert not errors, errors
+    assert plan.device_status(stream=st) == 0
+    ro, rl = refs[id(w)]
+    first = results[0][0][0].cpu()
+    for k in (0, 1):
+        for out, lse in results[k]:
+            assert torch.equal(out.cpu(), first)
+    out, lse = results[1][-1]
+    assert_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, w.dtype, what="shared plan")

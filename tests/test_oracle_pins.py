@@ -258,10 +258,34 @@ def pin_gather_walk_golden():
     return bool(ok)
 
 
+def pin_sampled_rows():
+    """attention_rows (the sampled-row form the full-size checks use) against
+    torch's scaled_dot_product_attention on contiguous K/V and against the
+    whole-batch oracle, element by element.  The batch puts empty requests
+    (qo_len 0) between non-empty ones and ends on a one-row request, so rows
+    at every request boundary are mapped to their request; G = 2, causal
+    and not, pages permuted; rows are asked for out of order."""
+    ok = True
+    for causal in (True, False):
+        w = small([2, 0, 3, 0, 0, 1, 4, 1], [5, 4, 7, 3, 1, 9, 6, 2], 4, 2, causal=causal, seed=23)
+        T = int(w.qo_indptr[-1])
+        rows = [(r, h) for r in range(T) for h in range(w.num_qo_heads)]
+        order = np.random.default_rng(5).permutation(len(rows))
+        rows = [rows[i] for i in order]
+        got = A.attention_rows(w, rows)
+        ro, rl = dense_reference(w)
+        fo, fl = A.attention(w)
+        for (r, h) in rows:
+            o, l = got[(r, h)]
+            ok &= close(o, ro[r, h], 1e-12) and abs(l - rl[r, h]) <= 1e-12
+            ok &= close(o, fo[r, h], 1e-12) and abs(l - fl[r, h]) <= 1e-12
+    return bool(ok)
+
+
 PINS = [pin_sdpa_contiguous, pin_walk_equals_gather, pin_single_key_returns_v, pin_constant_v,
         pin_zero_query, pin_two_keys_closed_form, pin_page_permutation, pin_prefix_sharing,
         pin_decode_equals_last_prefill_row, pin_padded_equals_unpadded, pin_split_merge,
-        pin_kv_len_matches_generator, pin_gather_walk_golden]
+        pin_kv_len_matches_generator, pin_gather_walk_golden, pin_sampled_rows]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=[p.__name__ for p in PINS])
@@ -305,6 +329,11 @@ MUTANTS = {
     "slot_swapped": ("locate", lambda pages, t, ps: (int(pages[t % len(pages)]), t // len(pages) % ps)),
     "kv_len_ignores_last": ("kv_len_of", lambda n, last, ps: n * ps),
     "lse_base2": ("softmax_stats", lambda s: (lambda m: (m + math.log2(np.sum(np.exp(s - m))), np.exp(s - m) / np.sum(np.exp(s - m))))(float(np.max(s)))),
+    # sampled rows: a row at a request boundary given to the request before it
+    "row_request_left": ("request_of_row",
+                         lambda qo_indptr, row: int(np.searchsorted(np.asarray(qo_indptr), row, side="left") - 1)),
+    # sampled rows: the first request's row index used for every request
+    "row_request_first": ("request_of_row", lambda qo_indptr, row: 0),
     "no_max_shift_weights": ("softmax_stats", lambda s: (float(np.max(s)) + math.log(np.sum(np.exp(s - np.max(s)))), np.exp(s - np.max(s)))),
 }
 

@@ -35,7 +35,7 @@ def test_exports_every_declared_symbol(lib):
     assert sorted(decl) == sorted(pa.EXPORTED)
     for name in decl:
         assert hasattr(lib, name), name
-    assert pa.version() == "0.1.0"
+    assert pa.version() == "0.2.0"
 
 
 def _ref(w, **kw):

@@ -182,12 +182,13 @@ def tiny() -> Workload:
                     np.asarray(kv, np.int64))
 
 
-def decode(batch_size: int = 128, seq_len: int = 1024) -> Workload:
+def decode(batch_size: int = 128, seq_len: int = 1024, num_qo_heads: int = 8) -> Workload:
     """The decode script's batch: ``batch_size`` requests, 1 query token
     each, ``seq_len`` keys, Hq 8 / Hkv 1, head_dim 128, page_size 16, page ids
-    0..P-1 in order (each request owns a contiguous run of 64 pages)."""
+    0..P-1 in order (each request owns a contiguous run of 64 pages).
+    ``num_qo_heads`` re-heads it (profiling other group sizes)."""
     s = _SEEDS["decode"]
-    ps, Hq, Hkv, D = 16, 8, 1, 128
+    ps, Hq, Hkv, D = 16, int(num_qo_heads), 1, 128
     pages_per_seq = pages_for(seq_len, ps)
     P = pages_per_seq * batch_size
     tabs = build_tables([1] * batch_size, [seq_len] * batch_size, ps, np.arange(P, dtype=np.int32))
