@@ -321,6 +321,10 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_err(e, "cudaGetDevice");
   if (dev != plan->device) return set_err(PA_ERR_INVALID_ARG, "current device differs from the plan's device");
+  // make the device's primary context current on this thread: a thread whose
+  // first library call is run has none yet, and encoding a tensor map needs one
+  e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return cuda_err(e, "cudaSetDevice");
 
   // the tensor maps of the last pointers seen are cached in the plan; the
   // launches below use copies taken under the plan's lock, so host threads

@@ -96,16 +96,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t addr, uint32_t parity) {
   return ok != 0;
 }
 
+// Non-blocking probe of the same phase (try_wait may suspend the thread for
+// a hardware-chosen while before it reports an incomplete phase).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Below this many cycles a wait limit polls with non-blocking probes, so that
+// the limit and not try_wait's own suspension decides when it gives up.
+constexpr long long kShortWaitLimit = 1000000;
+
 // Bounded wait for the phase with the given parity to complete.  Returns
 // false (and records PA_DEV_TIMEOUT, and raises *abort_flag) when `limit`
 // clock cycles pass or when *abort_flag is already raised by another thread.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
                                           int32_t* status, long long limit) {
   const uint32_t a = smem_u32(bar);
-  if (mbar_try_wait(a, parity)) return true;
+  const bool probe = limit < kShortWaitLimit;
+  if (probe ? mbar_test_wait(a, parity) : mbar_try_wait(a, parity)) return true;
   const long long t0 = clock64();
   while (true) {
-    if (mbar_try_wait(a, parity)) return true;
+    if (probe ? mbar_test_wait(a, parity) : mbar_try_wait(a, parity)) return true;
     if (*abort_flag) return false;
     if (clock64() - t0 > limit) {
       *abort_flag = 1;

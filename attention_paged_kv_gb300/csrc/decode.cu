@@ -91,11 +91,29 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
     const int br_shift = min(p.ps_shift, 6);
     const int BR = 1 << br_shift;  // rows per copy: a page, or 64 slots of it
     const uint32_t sbase = smem_u32(smem);
+    // TMA path: lane b copies box b (a page, or 64 slots of one) of every
+    // stage.  Its page id is read three stages ahead into one of three
+    // registers (the loop is unrolled by three, so no register of the ring
+    // is moved before its load lands), so that no global load sits between
+    // a free slot and the copy into it
+    auto stage_pid = [&](int jj) -> int {
+      if (!use_tma || jj >= nstage) return 0;
+      const int s0j = it.tok0 + jj * kDecTile;
+      const int nb = (min(s0j + kDecTile, it.tok1) - s0j + BR - 1) >> br_shift;
+      return lane < nb ? __ldg(p.pages + rq.page_start + ((s0j + lane * BR) >> p.ps_shift)) : 0;
+    };
+    int pids[3] = {stage_pid(0), stage_pid(1), stage_pid(2)};
     int issued = 0;
-    for (int j = 0; j < nstage; ++j) {
+    bool ok = true;
+    for (int j0 = 0; ok && j0 < nstage; j0 += 3) {
+#pragma unroll
+     for (int u = 0; u < 3; ++u) {
+      const int j = j0 + u;
+      if (!ok || j >= nstage) break;
       const int st = j % kDecStages;
+      int pid = pids[u];
+      pids[u] = stage_pid(j + 3);
       if (j >= kDecStages) {
-        bool ok = true;
         if (lane == 0) ok = mbar_wait(&empty[st], ((j / kDecStages) - 1) & 1, abort_flag, p.status, p.wait_limit);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -107,18 +125,17 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
         const int nbox = (s1 - s0 + BR - 1) >> br_shift;
         if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(nbox * BR * 128 * NKB * 2));
         __syncwarp();
-        for (int b = lane; b < nbox; b += 32) {
-          const KvLoc loc = kv_locate(p.pages, rq.page_start, s0 + b * BR, p.ps_shift);
-          int pid = loc.page;
+        if (lane < nbox) {
+          const int slot = (s0 + lane * BR) & (p.ps - 1);
           if (static_cast<unsigned>(pid) >= static_cast<unsigned>(p.num_pages)) {
             atomicOr(p.status, PA_DEV_BAD_INDEX);
             pid = 0;
           }
 #pragma unroll
           for (int kb = 0; kb < NKB; ++kb) {
-            tma_kv_rows(kdst + kb * C::BLK + b * BR * 128, &kv_map, kb * 64, it.kv_head, loc.slot, 2 * pid,
+            tma_kv_rows(kdst + kb * C::BLK + lane * BR * 128, &kv_map, kb * 64, it.kv_head, slot, 2 * pid,
                         &full[st], p.hnd);
-            tma_kv_rows(kdst + C::STAGE_K + kb * C::BLK + b * BR * 128, &kv_map, kb * 64, it.kv_head, loc.slot,
+            tma_kv_rows(kdst + C::STAGE_K + kb * C::BLK + lane * BR * 128, &kv_map, kb * 64, it.kv_head, slot,
                         2 * pid + 1, &full[st], p.hnd);
           }
         }
@@ -149,6 +166,7 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
         mbar_arrive(&full[st]);
       }
       issued = j + 1;
+     }
     }
     if (use_tma && lane == 0) {
       for (int j = max(0, issued - kDecStages); j < issued; ++j) {

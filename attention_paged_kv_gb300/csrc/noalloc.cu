@@ -79,6 +79,9 @@ extern "C" pagedattn_status pagedattn_run_decode_noalloc(pagedattn_plan_t plan, 
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_err(e, "cudaGetDevice");
+  // the device's primary context current on this thread (tensor-map encoding needs one)
+  e = cudaSetDevice(dev);
+  if (e != cudaSuccess) return cuda_err(e, "cudaSetDevice");
   void* scratch = nullptr;
   pagedattn_status s = scratch_address(dev, &scratch);
   if (s != PA_OK) return s;

@@ -21,7 +21,10 @@
 //   warp 9     MMA issuer (one thread) and TMEM owner.
 //
 // K and V tiles have separate two-slot rings (four for head_dim 64), so the
-// next K tile loads as soon as both S MMAs have read the slot it reuses.
+// next K tile loads as soon as both S MMAs have read the slot it reuses.  The
+// producer reads each tile's page ids two tiles ahead: with the page-table
+// read between a slot becoming free and its copy, the producer had set the
+// pace of the whole CTA (a key-tile period of ~4000 SM cycles against ~3700).
 //
 // TMEM (512 columns): S_A at 0, S_B at 128 (fp32 128x128), O_A at 256, O_B at
 // 384 (fp32 128xD).  P (fp16/bf16, two per column) is written over the first
@@ -32,7 +35,8 @@
 // takes 256 columns a tile, and batches of short prompts, where two CTAs to
 // an SM hide each other's fixed costs (Q and first K/V loads, epilogue).
 //
-// Per key tile j the MMA thread issues, in order:
+// Per key tile j the MMA thread (which polls its barriers rather than
+// sleeping on them) issues, in order:
 //   PV_A(j) ; S_A(j+1) ; PV_B(j) ; S_B(j+1)
 // so while the softmax warps of one tile turn S into P, the tensor core works
 // on the other tile.  Softmax per tile: the S row is read from TMEM into
@@ -103,6 +107,25 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
   return __all_sync(0xffffffffu, ok);
 }
 
+// Bounded wait that polls with non-blocking probes and never suspends: the
+// MMA thread waits this way, since waking a suspended thread cost ~1.8 % of
+// the prefill (the softmax warps, which share their SM sub-partitions with the
+// other tile's softmax, wait with try_wait: spinning there cost 3.6 %).
+__device__ __forceinline__ bool spin_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
+                                          int32_t* status, long long limit) {
+  const uint32_t a = smem_u32(bar);
+  if (mbar_test_wait(a, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_test_wait(a, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      *abort_flag = 1;
+      atomicOr(status, PA_DEV_TIMEOUT);
+      return false;
+    }
+  }
+}
 // Wait that ignores the abort flag (used to drain in-flight async work).
 __device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
   const uint32_t a = smem_u32(bar);
@@ -144,7 +167,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
   uint64_t* q_full = bars + 4 * NST;    // both Q tiles landed
   uint64_t* s_full = q_full + 1;        // [2] S_x MMA done
   uint64_t* p_full = s_full + 2;        // [2] P_x (and O_x correction) written
-  uint64_t* o_done = p_full + 2;        // [2] PV_x MMA done
+  uint64_t* o_done = p_full + 2;        // [2] the last PV_x MMA done (one phase)
   uint64_t* fin = o_done + 2;           // all MMAs retired (teardown)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
@@ -198,14 +221,35 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       }
     }
     const int ps = p.ps, sh = p.ps_shift;
-    // tile j: K into slot j % NST once S_A(j - NST), S_B(j - NST) are done with
-    // it, then V once PV_A(j - NST), PV_B(j - NST) are
+    // TMA path: lane l gathers page l of every key tile (at most 16 pages of
+    // >= 8 slots).  Its page id is read three tiles ahead into one of three
+    // registers (the loop is unrolled by three, so the ring never moves a
+    // register that a load has not filled yet), so that no global load sits
+    // between a slot becoming free and the copy into it: with the load in
+    // between, the producer set the pace of the whole CTA.
+    auto tile_pid = [&](int jj) -> int {
+      if (!use_tma || jj >= nkt) return 0;
+      const int k0j = it.kv_tok0 + jj * kKvTile;
+      const int kendj = min(k0j + kKvTile, it.kv_tok1);
+      const int npgj = ((kendj - 1) >> sh) - (k0j >> sh) + 1;
+      return lane < npgj ? __ldg(p.pages + rq.page_start + (k0j >> sh) + lane) : 0;
+    };
+    int pid_j = tile_pid(0), pid_j1 = tile_pid(1);
     int issued_k = 0, issued_v = 0;
-    for (int j = 0; j < nkt; ++j) {
+    bool ok = true;
+    for (int j = 0; ok && j < nkt; ++j) {
+     {
       const int st = j % NST;
       const int k0 = it.kv_tok0 + j * kKvTile;
       const int kend = min(k0 + kKvTile, it.kv_tok1);
-      bool ok = true;
+      const int pid_j2 = tile_pid(j + 2);
+      int pid = pid_j;
+      if (use_tma && static_cast<unsigned>(pid) >= static_cast<unsigned>(p.num_pages)) {
+        atomicOr(p.status, PA_DEV_BAD_INDEX);
+        pid = 0;
+      }
+      pid_j = pid_j1;
+      pid_j1 = pid_j2;
       for (int half = 0; half < 2 && ok; ++half) {  // 0: K, 1: V
         uint64_t* empty = half ? empty_v : empty_k;
         uint64_t* full = half ? full_v : full_k;
@@ -220,16 +264,10 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
           const int npg = ((kend - 1) >> sh) - pg0 + 1;
           if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(npg * ps * 128 * NKB));
           __syncwarp();
-          for (int l = lane; l < npg; l += 32) {
-            const KvLoc loc = kv_locate(p.pages, rq.page_start, k0 + l * ps, sh);
-            int pid = loc.page;
-            if (static_cast<unsigned>(pid) >= static_cast<unsigned>(p.num_pages)) {
-              atomicOr(p.status, PA_DEV_BAD_INDEX);
-              pid = 0;
-            }
+          if (lane < npg) {
 #pragma unroll
             for (int kb = 0; kb < NKB; ++kb)
-              tma_kv_rows(dst0 + kb * C::BLK + l * ps * 128, &kv_map, kb * 64, it.kv_head, 0, 2 * pid + half,
+              tma_kv_rows(dst0 + kb * C::BLK + lane * ps * 128, &kv_map, kb * 64, it.kv_head, 0, 2 * pid + half,
                           &full[st], p.hnd);
           }
         } else {
@@ -263,7 +301,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
         }
         if (half) issued_v = j + 1; else issued_k = j + 1;
       }
-      if (!ok) break;
+     }
     }
     // drain: copies still in flight must land before the CTA's memory goes away
     if (lane == 0) {
@@ -304,13 +342,13 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
                       id_o, 1u);
           }
         }
-        tc_commit(&o_done[x]);
+        if (j == nkt - 1) tc_commit(&o_done[x]);  // the epilogue's only wait on O
       };
       // tile A's P_lo of the first key tile may live in K slot 0: then that
       // slot is released only once PV_A(0) has read it
       const bool plo_in_k = lo_split0 && (C::OFF_PLO_A == C::OFF_K);
-      bool ok = mbar_wait(q_full, 0, abort_flag, p.status, p.wait_limit);
-      if (ok) ok = mbar_wait(&full_k[0], 0, abort_flag, p.status, p.wait_limit);
+      bool ok = spin_wait(q_full, 0, abort_flag, p.status, p.wait_limit);
+      if (ok) ok = spin_wait(&full_k[0], 0, abort_flag, p.status, p.wait_limit);
       if (ok) {
         tc_fence_after();
         issue_s(0, 0);
@@ -321,21 +359,21 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
         const int st = j % NST;
         const bool more = j + 1 < nkt;
         const int st1 = (j + 1) % NST;
-        ok = mbar_wait(&p_full[0], j & 1, abort_flag, p.status, p.wait_limit);
-        if (ok) ok = mbar_wait(&full_v[st], (j / NST) & 1, abort_flag, p.status, p.wait_limit);
+        ok = spin_wait(&p_full[0], j & 1, abort_flag, p.status, p.wait_limit);
+        if (ok) ok = spin_wait(&full_v[st], (j / NST) & 1, abort_flag, p.status, p.wait_limit);
         if (!ok) break;
         tc_fence_after();
         issue_pv(0, j, st);
         if (j == 0 && plo_in_k) tc_commit(&empty_k[0]);
         if (more) {
-          ok = mbar_wait(&full_k[st1], ((j + 1) / NST) & 1, abort_flag, p.status, p.wait_limit);
+          ok = spin_wait(&full_k[st1], ((j + 1) / NST) & 1, abort_flag, p.status, p.wait_limit);
           if (!ok) break;
           tc_fence_after();
           issue_s(0, st1);
           if (!has_b) tc_commit(&empty_k[st1]);
         }
         if (has_b) {
-          ok = mbar_wait(&p_full[1], j & 1, abort_flag, p.status, p.wait_limit);
+          ok = spin_wait(&p_full[1], j & 1, abort_flag, p.status, p.wait_limit);
           if (!ok) break;
           tc_fence_after();
           issue_pv(1, j, st);
@@ -403,8 +441,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       float m5[5];
 #pragma unroll
       for (int u = 0; u < 5; ++u) m5[u] = fmax3(m15[3 * u], m15[3 * u + 1], m15[3 * u + 2]);
-      float mx = fmax3(fmax3(m5[0], m5[1], m5[2]), m5[3], m5[4]);
-      const float mx2 = mx * sl2;
+      const float mx2 = fmax3(fmax3(m5[0], m5[1], m5[2]), m5[3], m5[4]) * sl2;
       float alpha = 1.f;
       bool resc = false;
       if (mx2 > m_ref + 8.f) {
@@ -425,8 +462,11 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
 
       // p = exp2(s * scale_log2 - m), row sum, P (hi) into TMEM over S.  The
       // row sum runs in two independent chains (one long chain of dependent
-      // adds would set the pace; more chains cost registers).  The first key tile of a sequence is
-      // compiled apart: only there may P be split into hi + lo.
+      // adds would set the pace; more chains cost registers).  The first key
+      // tile of a sequence is compiled apart: only there may P be split into
+      // hi + lo.  (Measured slower and left out: a quarter or more of the
+      // exponentials on the FMA pipe by a polynomial, and exponentials
+      // against the running maximum with the tile maximum taken alongside.)
       const float2 sc2 = make_float2(sl2, sl2), nm2 = make_float2(-m_use, -m_use);
       auto softmax_p = [&](auto first_tag) -> float {
         constexpr bool kFirst = decltype(first_tag)::value;
@@ -463,13 +503,9 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
         return sum.x + sum.y;
       };
       const float rs = (j == 0) ? softmax_p(std::true_type{}) : softmax_p(std::false_type{});
-      // S_x(j) done implies PV_x(j-1) done (the MMAs run in issue order); the
-      // barrier makes O's contents visible before it is rescaled
-      if (j >= 1) {
-        ok = warp_wait(&o_done[x], (j - 1) & 1, abort_flag, p.status, p.wait_limit);
-        if (!ok) break;
-        tc_fence_after();
-      }
+      // PV_x(j-1) is complete here: it was issued before S_x(j), and the
+      // commit that completed s_full for S_x(j) tracks every MMA issued
+      // before it, so O may be rescaled without a wait of its own
       if (__any_sync(0xffffffffu, resc)) {
 #pragma unroll
         for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -508,7 +544,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     }
 
     // ---------------------------------------------------------------- epilogue
-    if (ok && (x == 0 || has_b)) ok = warp_wait(&o_done[x], (nkt - 1) & 1, abort_flag, p.status, p.wait_limit);
+    if (ok && (x == 0 || has_b)) ok = warp_wait(&o_done[x], 0, abort_flag, p.status, p.wait_limit);
     if (ok && (x == 0 || has_b)) {
       tc_fence_after();
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;

@@ -463,7 +463,7 @@ def test_cascade_shared_prefix_decode(cuda_cores):
 @pytest.mark.parametrize("name,opts", [
     ("tiny", {}), ("tiny", {"force_prefill": True}), ("tiny", {"force_prefill": True, "prefill_q_tiles": 1}),
     ("tiny", {"force_cp_async": True, "force_prefill": True}),
-    ("decode", {"decode_chunk_pages": 4}), ("decode", {"decode_cuda_cores": True, "decode_chunk_pages": 4})])
+    ("decode", {"decode_chunk_pages": 64}), ("decode", {"decode_cuda_cores": True, "decode_chunk_pages": 64})])
 def test_wait_limit_gives_up_then_normal_run(name, opts):
     """Every in-kernel pipeline wait is bounded.  With the bound cut to one
     clock cycle (the wait_limit_cycles test hook) the first wait that finds
