@@ -860,7 +860,7 @@ cudaError_t launch_mma(const RunArgs& a, const CUtensorMap* map, const KParams& 
 template <typename T, int D>
 cudaError_t launch_decode_d(const RunArgs& a, const CUtensorMap* map, const KParams& kp) {
   const HostPlan& hp = *a.hp;
-  const int use_tma = (map != nullptr && hp.ps >= 8) ? 1 : 0;
+  const int use_tma = (map != nullptr && hp.ps >= 8 && !a.force_cp_async) ? 1 : 0;
   CUtensorMap dummy;
   memset(&dummy, 0, sizeof(dummy));
   const CUtensorMap* m = use_tma ? map : &dummy;

@@ -407,10 +407,14 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = (x == 0) || has_b;
 
-    for (int j = 0; ok && j < nkt; ++j) {
+    // One key tile of the online softmax; the first tile of the item (the
+    // only one where P may be split into hi + lo) is a separate instance, so
+    // that the loop over the others carries only the common path (with both
+    // in the loop body the row's registers spilled on every tile).
+    auto tile = [&](int j, auto first_tag) -> bool {
       const int k0 = it.kv_tok0 + j * kKvTile;
       ok = warp_wait(&s_full[x], j & 1, abort_flag, p.status, p.wait_limit);
-      if (!ok) break;
+      if (!ok) return false;
       tc_fence_after();
       const int lim = row_end - k0;
 
@@ -453,11 +457,12 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       }
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
 
-      const bool lo_split = lo_split0 && j == 0;
+      constexpr bool kFirstTile = decltype(first_tag)::value;
+      const bool lo_split = kFirstTile && lo_split0;
       if (lo_split && x == 0 && C::OFF_PLO_A == C::OFF_K && has_b) {
         // tile A's P_lo reuses K stage 0: S_B(0) must be done reading it
         ok = warp_wait(&s_full[1], 0, abort_flag, p.status, p.wait_limit);
-        if (!ok) break;
+        if (!ok) return false;
       }
 
       // p = exp2(s * scale_log2 - m), row sum, P (hi) into TMEM over S.  The
@@ -502,7 +507,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
         const float2 sum = __fadd2_rn(acc[0], acc[1]);
         return sum.x + sum.y;
       };
-      const float rs = (j == 0) ? softmax_p(std::true_type{}) : softmax_p(std::false_type{});
+      const float rs = softmax_p(first_tag);
       // PV_x(j-1) is complete here: it was issued before S_x(j), and the
       // commit that completed s_full for S_x(j) tracks every MMA issued
       // before it, so O may be rescaled without a wait of its own
@@ -524,7 +529,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
         if (valid < kKvTile) {
           const int st = j % NST;
           ok = warp_wait(&full_v[st], (j / NST) & 1, abort_flag, p.status, p.wait_limit);
-          if (!ok) break;
+          if (!ok) return false;
           if (r >= valid) {
             uint8_t* vrow = smem + C::OFF_V + st * C::KV_BYTES + r * 128;
 #pragma unroll
@@ -541,7 +546,10 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&p_full[x]);
-    }
+      return true;
+    };
+    if (ok && nkt > 0) ok = tile(0, std::true_type{});
+    for (int j = 1; ok && j < nkt; ++j) ok = tile(j, std::false_type{});
 
     // ---------------------------------------------------------------- epilogue
     if (ok && (x == 0 || has_b)) ok = warp_wait(&o_done[x], 0, abort_flag, p.status, p.wait_limit);

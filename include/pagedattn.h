@@ -80,7 +80,7 @@ typedef struct {
   int32_t force_prefill;       /* 1: every request uses the tcgen05 prefill kernel    */
   int32_t decode_chunk_pages;  /* > 0: pages per decode split (default: see plan)    */
   int32_t prefill_chunk_tiles; /* > 0: 128-key tiles per prefill split               */
-  int32_t force_cp_async;      /* 1: stage prefill K/V with cp.async instead of TMA   */
+  int32_t force_cp_async;      /* 1: stage K/V with cp.async instead of TMA           */
   int32_t decode_cuda_cores;   /* 1: single-token requests at group sizes <= 8 run on
                                   the CUDA-core decode kernel, and multi-token
                                   requests all go to the prefill kernel (default:

@@ -556,3 +556,17 @@ def test_host_threads():
             assert torch.equal(out.cpu(), first)
     out, lse = results[1][-1]
     assert_close(out.double().cpu().numpy(), lse.double().cpu().numpy(), ro, rl, w.dtype, what="shared plan")
+
+
+@pytest.mark.parametrize("G", [2, 8])
+def test_decode_cp_async_equals_tma(G):
+    """Decode staged by cp.async (force_cp_async) writes the same shared-memory
+    tiles as the TMA path, so the outputs are identical bit for bit; both
+    match the oracle."""
+    w = workloads.make_custom("dcp", [1] * 9, [1, 15, 16, 17, 300, 1000, 64, 129, 2000], 2 * G, 2, 128, 16,
+                              dtype=torch.bfloat16, seed=G)
+    ro, rl = A.attention(w)
+    o1, l1, _ = run(w, decode_chunk_pages=8)
+    o2, l2, _ = run(w, decode_chunk_pages=8, force_cp_async=True)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    assert_close(o1, l1, ro, rl, w.dtype, what=f"decode G{G}")
