@@ -110,7 +110,9 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volati
 // Bounded wait that polls with non-blocking probes and never suspends: the
 // MMA thread waits this way, since waking a suspended thread cost ~1.8 % of
 // the prefill (the softmax warps, which share their SM sub-partitions with the
-// other tile's softmax, wait with try_wait: spinning there cost 3.6 %).
+// other tile's softmax, wait with try_wait: spinning there cost 3.6 %, and
+// neither a suspend-time hint for them nor a back-off for the MMA thread
+// changed anything).
 __device__ __forceinline__ bool spin_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort_flag,
                                           int32_t* status, long long limit) {
   const uint32_t a = smem_u32(bar);
@@ -317,29 +319,36 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     if (lane == 0) {
       const uint32_t id_s = idesc_f16(Elt<T>::kBf16, 0, 0, 128, 128);
       const uint32_t id_o = idesc_f16(Elt<T>::kBf16, 0, 1, 128, D);
+      // Matrix descriptors of each operand's first k-step, made once: a
+      // k-step (or another tile or stage) adds its byte offset / 16 to the
+      // start-address field (shared addresses stay below 2^18, so the sum
+      // never carries out of the field).
+      const uint64_t dq0 = smem_desc_sw128(q_addr(0), 16, 1024);
+      const uint64_t dk0 = smem_desc_sw128(k_addr(0), 16, 1024);
+      const uint64_t dv0 = smem_desc_sw128(v_addr(0), C::BLK, 1024);
       auto issue_s = [&](int x, int st) {
         const uint32_t d = tmem + x * 128;
+        const uint64_t qd = dq0 + uint64_t(x) * (C::Q_BYTES >> 4);
+        const uint64_t kd = dk0 + uint64_t(st) * (C::KV_BYTES >> 4);
 #pragma unroll
         for (int k = 0; k < D / 16; ++k) {
-          const uint32_t koff = (k >> 2) * C::BLK + (k & 3) * 32;
-          tc_mma_ss(d, smem_desc_sw128(q_addr(x) + koff, 16, 1024), smem_desc_sw128(k_addr(st) + koff, 16, 1024),
-                    id_s, k > 0 ? 1u : 0u);
+          const uint32_t koff = ((k >> 2) * C::BLK + (k & 3) * 32) >> 4;
+          tc_mma_ss(d, qd + koff, kd + koff, id_s, k > 0 ? 1u : 0u);
         }
         tc_commit(&s_full[x]);
       };
       auto issue_pv = [&](int x, int j, int st) {
         const uint32_t d = tmem + C::O_COL + x * 128;
+        const uint64_t vd = dv0 + uint64_t(st) * (C::KV_BYTES >> 4);
 #pragma unroll
         for (int k = 0; k < kKvTile / 16; ++k)
-          tc_mma_ts(d, tmem + x * 128 + k * 8, smem_desc_sw128(v_addr(st) + k * 2048, C::BLK, 1024), id_o,
-                    (j > 0 || k > 0) ? 1u : 0u);
+          tc_mma_ts(d, tmem + x * 128 + k * 8, vd + (k * 2048 >> 4), id_o, (j > 0 || k > 0) ? 1u : 0u);
         if (j == 0 && lo_split0) {
           const uint32_t lo = sbase + plo_off(x);
 #pragma unroll
           for (int k = 0; k < kKvTile / 16; ++k) {
             const uint32_t aoff = (k >> 2) * C::BLK + (k & 3) * 32;
-            tc_mma_ss(d, smem_desc_sw128(lo + aoff, 16, 1024), smem_desc_sw128(v_addr(st) + k * 2048, C::BLK, 1024),
-                      id_o, 1u);
+            tc_mma_ss(d, smem_desc_sw128(lo + aoff, 16, 1024), vd + (k * 2048 >> 4), id_o, 1u);
           }
         }
         if (j == nkt - 1) tc_commit(&o_done[x]);  // the epilogue's only wait on O
