@@ -79,11 +79,15 @@ __device__ __forceinline__ uint32_t sw_off(int t, int c) {
 // Producer warp of the decode kernels: streams the item's keys in 64-key
 // stages (K then V, 128-byte-swizzled rows) into kDecStages buffers, by TMA
 // through the page table or, for pages of fewer than 8 slots, by cp.async.
-// On return every copy it issued has landed (or its wait gave up).
+// With TMA it copies the halves [h0, h1) of each stage (0 = K, 1 = V), so two
+// producer warps can share a stage's copies; each then arrives on the
+// stage's full barrier with its own byte count.  On return every copy it
+// issued has landed (or its wait gave up).
 template <typename T, int D>
 __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const KParams& p, const DecItem& it,
                                                const ReqEntry& rq, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                                               volatile int32_t* abort_flag, int use_tma, int nstage, int lane) {
+                                               volatile int32_t* abort_flag, int use_tma, int nstage, int lane,
+                                               int h0 = 0, int h1 = 2) {
   using C = DecCfg<D>;
   constexpr int NKB = C::NKB;
   constexpr int NCH = D / 8;
@@ -123,7 +127,7 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
       const uint32_t kdst = sbase + st * C::STAGE;
       if (use_tma) {
         const int nbox = (s1 - s0 + BR - 1) >> br_shift;
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(nbox * BR * 128 * NKB * 2));
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(nbox * BR * 128 * NKB * (h1 - h0)));
         __syncwarp();
         if (lane < nbox) {
           const int slot = (s0 + lane * BR) & (p.ps - 1);
@@ -133,10 +137,12 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
           }
 #pragma unroll
           for (int kb = 0; kb < NKB; ++kb) {
-            tma_kv_rows(kdst + kb * C::BLK + lane * BR * 128, &kv_map, kb * 64, it.kv_head, slot, 2 * pid,
-                        &full[st], p.hnd);
-            tma_kv_rows(kdst + C::STAGE_K + kb * C::BLK + lane * BR * 128, &kv_map, kb * 64, it.kv_head, slot,
-                        2 * pid + 1, &full[st], p.hnd);
+            if (h0 == 0)
+              tma_kv_rows(kdst + kb * C::BLK + lane * BR * 128, &kv_map, kb * 64, it.kv_head, slot, 2 * pid,
+                          &full[st], p.hnd);
+            if (h1 == 2)
+              tma_kv_rows(kdst + C::STAGE_K + kb * C::BLK + lane * BR * 128, &kv_map, kb * 64, it.kv_head, slot,
+                          2 * pid + 1, &full[st], p.hnd);
           }
         }
       } else {
@@ -180,8 +186,8 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
 }
 
 template <typename T, int D, int G>
-__global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p,
-                                               const int use_tma) {
+__global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
+    decode_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p, const int use_tma) {
   using C = DecCfg<D>;
   constexpr int NKB = C::NKB;
   constexpr int NCH = D / 8;       // 16-byte chunks per row
@@ -435,8 +441,12 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1)) decode
 // small-query variant of the prefill kernel as missing.  Here the packed rows
 // r = token * G + head of an item are the M rows of m16n8k16 fragments, so
 // S = q K^T needs no reshaping:
-//   warp 4     the producer of the CUDA-core kernel (64-key stages, 128-byte
-//              swizzled rows, TMA or cp.async).
+//   warps 4-5  the producer of the CUDA-core kernel (64-key stages, 128-byte
+//              swizzled rows), split in two: warp 4 copies the stages' K,
+//              warp 5 their V (each TMA copy costs its issuing thread ~90
+//              cycles when the data comes from HBM, and one warp issuing
+//              all copies limited a CTA's stream: mixed-batch decode 0.712
+//              -> 0.698 ms).  With cp.async staging warp 4 copies both.
 //   warps 0-3  row group rg = warp % RGN (16 rows each), key subset
 //              kq = warp / RGN of every stage: with RGN row groups each warp
 //              takes 16 * RGN of the stage's 64 keys.  ldmatrix feeds K from
@@ -480,7 +490,8 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "memory");
 }
 
-constexpr int kDmThreads = 160;  // 4 MMA warps + 1 producer
+constexpr int kDmProds = 2;                        // producer warps: one copies K, one V
+constexpr int kDmThreads = 32 * (4 + kDmProds);    // 4 MMA warps + producer(s)
 
 template <int RC>
 struct RowClass {
@@ -514,7 +525,7 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
 
   if (tid == 0) {
     for (int i = 0; i < kDecStages; ++i) {
-      mbar_init(&full[i], use_tma ? 1 : 32);
+      mbar_init(&full[i], use_tma ? kDmProds : 32);
       mbar_init(&empty[i], 4);
     }
     *abort_flag = 0;
@@ -522,8 +533,14 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
   }
   __syncthreads();
 
-  if (warp == 4) {
-    decode_produce<T, D>(kv_map, p, it, rq, smem, full, empty, abort_flag, use_tma, nstage, lane);
+  if (warp >= 4) {
+    // with two producer warps and TMA staging, warp 4 copies K and warp 5 V;
+    // cp.async staging (pages of < 8 slots) stays with warp 4 alone
+    if (warp == 4 || use_tma) {
+      const int h0 = (kDmProds == 2 && use_tma && warp == 5) ? 1 : 0;
+      const int h1 = (kDmProds == 2 && use_tma && warp == 4) ? 1 : 2;
+      decode_produce<T, D>(kv_map, p, it, rq, smem, full, empty, abort_flag, use_tma, nstage, lane, h0, h1);
+    }
     asm volatile("bar.arrive 1, %0;" ::"n"(kDmThreads) : "memory");
     return;
   }
@@ -904,10 +921,13 @@ cudaError_t launch_decode(const RunArgs& a, const CUtensorMap* map_rows) {
   kp.n_items = a.hp->n_dec;
   const bool bf = a.hp->dtype == PA_BF16;
   if (a.hp->D == 128)
-    return bf ? launch_decode_d<__nv_bfloat16, 128>(a, map_rows, kp) : launch_decode_d<__half, 128>(a, map_rows, kp);
+    return bf ? launch_decode_d<__nv_bfloat16, 128>(a, map_rows, kp)
+              : launch_decode_d<__half, 128>(a, map_rows, kp);
   if (a.hp->D == 256)
-    return bf ? launch_decode_d<__nv_bfloat16, 256>(a, map_rows, kp) : launch_decode_d<__half, 256>(a, map_rows, kp);
-  return bf ? launch_decode_d<__nv_bfloat16, 64>(a, map_rows, kp) : launch_decode_d<__half, 64>(a, map_rows, kp);
+    return bf ? launch_decode_d<__nv_bfloat16, 256>(a, map_rows, kp)
+              : launch_decode_d<__half, 256>(a, map_rows, kp);
+  return bf ? launch_decode_d<__nv_bfloat16, 64>(a, map_rows, kp)
+            : launch_decode_d<__half, 64>(a, map_rows, kp);
 }
 
 cudaError_t launch_merge(const RunArgs& a) {

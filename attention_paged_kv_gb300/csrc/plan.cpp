@@ -24,9 +24,13 @@
 //  3. Decode split ("kv-parallelism" / split-k in the same issue): chunk c0 =
 //     clamp(ceil(P_dec / (4 * SMs)), 256 keys, 2048 keys) in whole pages,
 //     P_dec = sum of decode pages x Hkv.  With N(c) = sum over (request,
-//     kv head) of ceil(pages_b / c) items: if N(c0) exceeds one wave of
-//     2 * SMs resident CTAs but some c <= 2048 keys gives N(c) <= 2 * SMs,
-//     the smallest such c is taken (a small batch then runs in one wave).
+//     kv head) of ceil(pages_b / c) items, and hi = 2048 keys: if N(hi)
+//     fits one wave of 2 * SMs resident CTAs and covers at least 3/4 of the
+//     SMs, c = hi (splitting such a batch further only adds split states and
+//     a merge: the decode timing script's batch, 128 x 1024 keys, ran 17.5
+//     us split in two and 15.9 us whole on a GB300).  Else, if N(c0) exceeds
+//     one wave but some c <= hi gives N(c) <= 2 * SMs, the smallest such c is
+//     taken (a small batch then runs in one wave).
 //     Each (request, kv head) is cut into n = ceil(pages_b / c) splits of
 //     floor-spaced page boundaries (split s starts at page
 //     floor(s * pages_b / n)), so the splits of a request differ by at most
@@ -208,7 +212,9 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
         if (is_dec[b]) n += cdiv(req[b].np, c) * Hkv;
       return n;
     };
-    if (items_at(chunk) > wave && items_at(hi) <= wave) {
+    if (items_at(hi) <= wave && 4 * items_at(hi) >= int64_t(3) * in.num_sms) {
+      chunk = hi;
+    } else if (items_at(chunk) > wave && items_at(hi) <= wave) {
       int64_t a = chunk, z = hi;  // items_at(a) > wave >= items_at(z); items_at is nonincreasing
       while (z - a > 1) {
         const int64_t mid = (a + z) / 2;

@@ -68,8 +68,14 @@ constexpr float kLn2 = 0.6931471805599453f;
 template <int D, int NT>
 struct PreCfg {
   static_assert(NT == 1 || (NT == 2 && D <= 128), "two tiles need 2 x (128 + D) <= 512 TMEM columns");
-  static constexpr int THREADS = 32 * (4 * NT + 2);  // softmax warpgroup(s), producer, MMA issuer
+  // producers: two tiles have one warp for K and one for V (each TMA copy
+  // costs its issuing thread ~90 cycles, and one warp issuing all of a key
+  // tile's copies set the pace); one tile keeps one producer warp, so that
+  // two CTAs of 6 warps still fit an SM at 168 registers a thread
+  static constexpr int PRODS = NT == 2 ? 2 : 1;
+  static constexpr int THREADS = 32 * (4 * NT + 1 + PRODS);  // softmax warpgroup(s), MMA issuer, producer(s)
   static constexpr int WARP_PROD = 4 * NT, WARP_MMA = 4 * NT + 1;
+  static constexpr int WARP_PROD_V = PRODS == 2 ? 4 * NT + 2 : WARP_PROD;
   static constexpr int NKB = D / 64;                 // 128-byte column blocks of a row
   static constexpr int NST = NT == 1 ? 1 : (D == 128 ? 2 : 4);  // K/V pipeline stages
   static constexpr int BLK = 128 * 128;              // one 128-row x 128-byte block
@@ -208,9 +214,12 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == C::WARP_PROD) {
-    // ---------------------------------------------------------------- producer
-    if (lane == 0) {
+  if (warp == C::WARP_PROD || warp == C::WARP_PROD_V) {
+    // ---------------------------------------------------------------- producer(s)
+    // halves [h0, h1) of each key tile: 0 = K, 1 = V
+    const int h0 = (C::PRODS == 2 && warp == C::WARP_PROD_V) ? 1 : 0;
+    const int h1 = (C::PRODS == 2 && warp == C::WARP_PROD) ? 1 : 2;
+    if (warp == C::WARP_PROD && lane == 0) {
       tma_prefetch_desc(&q_map);
       if (use_tma) tma_prefetch_desc(&kv_map);
       mbar_arrive_expect_tx(q_full, uint32_t((has_b ? 2 : 1) * C::Q_BYTES));
@@ -224,11 +233,9 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     }
     const int ps = p.ps, sh = p.ps_shift;
     // TMA path: lane l gathers page l of every key tile (at most 16 pages of
-    // >= 8 slots).  Its page id is read three tiles ahead into one of three
-    // registers (the loop is unrolled by three, so the ring never moves a
-    // register that a load has not filled yet), so that no global load sits
-    // between a slot becoming free and the copy into it: with the load in
-    // between, the producer set the pace of the whole CTA.
+    // >= 8 slots).  Its page id is read two tiles ahead, so that no global
+    // load sits between a slot becoming free and the copy into it: with the
+    // load in between, the producer set the pace of the whole CTA.
     auto tile_pid = [&](int jj) -> int {
       if (!use_tma || jj >= nkt) return 0;
       const int k0j = it.kv_tok0 + jj * kKvTile;
@@ -252,7 +259,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       }
       pid_j = pid_j1;
       pid_j1 = pid_j2;
-      for (int half = 0; half < 2 && ok; ++half) {  // 0: K, 1: V
+      for (int half = h0; half < h1 && ok; ++half) {  // 0: K, 1: V
         uint64_t* empty = half ? empty_v : empty_k;
         uint64_t* full = half ? full_v : full_k;
         const uint32_t dst0 = half ? v_addr(st) : k_addr(st);
@@ -307,7 +314,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     }
     // drain: copies still in flight must land before the CTA's memory goes away
     if (lane == 0) {
-      drain_wait(q_full, 0);
+      if (warp == C::WARP_PROD) drain_wait(q_full, 0);
       if (use_tma) {
         for (int j = max(0, issued_k - NST); j < issued_k; ++j) drain_wait(&full_k[j % NST], (j / NST) & 1);
         for (int j = max(0, issued_v - NST); j < issued_v; ++j) drain_wait(&full_v[j % NST], (j / NST) & 1);

@@ -28,9 +28,11 @@ Rules (the planner is deterministic; nothing depends on timing):
    c0 = clamp(ceil(P_dec / target), lo = max(1, 256 // page_size),
    hi = max(1, 2048 // page_size)) pages.  Let N(c) = sum over decode
    requests of Hkv * ceil(pages_b / c), the item count at chunk c.  If
-   N(c0) > 2 * num_sms (more than one wave of resident CTAs) and
-   N(hi) <= 2 * num_sms, the chunk is the smallest c with N(c) <= 2 * num_sms;
-   else c0 (an override replaces both).  Request b is cut into
+   N(hi) <= 2 * num_sms and 4 * N(hi) >= 3 * num_sms (at chunk hi the items
+   fit one wave of resident CTAs and cover at least 3/4 of the SMs), the
+   chunk is hi.  Else, if N(c0) > 2 * num_sms (more than one wave) and
+   N(hi) <= 2 * num_sms, the chunk is the smallest c with
+   N(c) <= 2 * num_sms; else c0 (an override replaces all of these).  Request b is cut into
    n = ceil(pages_b / chunk) splits, split s covering pages
    [floor(s * pages_b / n), floor((s + 1) * pages_b / n)), for every kv head.
 4. Prefill items: 256 packed rows = (256 / G) query tokens x G heads (two
@@ -187,7 +189,9 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
         def n_items(c):
             return sum(Hkv * _cdiv(l[3], c) for l, d in zip(lens, is_dec) if d)
 
-        if n_items(chunk) > wave and n_items(hi) <= wave:
+        if n_items(hi) <= wave and 4 * n_items(hi) >= 3 * num_sms:
+            chunk = hi
+        elif n_items(chunk) > wave and n_items(hi) <= wave:
             chunk = next(c for c in range(chunk, hi + 1) if n_items(c) <= wave)
     part = 0
     dec, merges = [], []

@@ -447,12 +447,17 @@ def test_plan_ref_decode_script_split():
     blob = plan_ref.build(**{k: v for k, v in w.plan_args().items() if k != "causal"},
                           dtype=plan_ref.FP16, num_sms=148)
     h = plan_ref.decode_header(blob)
-    # 8192 pages / (4 * 148) -> 14, clamped up to 256 keys = 16 pages: 512 items, more than one
-    # wave of 2 * 148; the smallest chunk that fits one wave is 32 pages: 2 splits of 32 pages
-    assert h["dec_chunk_pages"] == 32 and h["n_dec"] == 256 and h["n_merge"] == 128
-    assert h["n_part_rows"] == 128 * 2 * 8 and h["n_pre"] == 0
+    # at the largest chunk (2048 keys = 128 pages) every request is one item: 128 items fit one
+    # wave of 2 * 148 and cover more than 3/4 of the 148 SMs, so no request is split
+    assert h["dec_chunk_pages"] == 128 and h["n_dec"] == 128 and h["n_merge"] == 0
+    assert h["n_part_rows"] == 0 and h["n_pre"] == 0
     dec, _, _ = plan_ref.items(blob)
-    assert sorted({(int(a), int(b)) for a, b in dec[:, 2:4]}) == [(0, 512), (512, 1024)]
+    assert sorted({(int(a), int(b)) for a, b in dec[:, 2:4]}) == [(0, 1024)]
+    # on 256 SMs the 128 items would leave half of them idle: split in two (one wave of 512)
+    blob = plan_ref.build(**{k: v for k, v in w.plan_args().items() if k != "causal"},
+                          dtype=plan_ref.FP16, num_sms=256)
+    h = plan_ref.decode_header(blob)
+    assert h["dec_chunk_pages"] == 16 and h["n_dec"] == 512 and h["n_merge"] == 128
 
 
 @pytest.mark.parametrize("kw", [{}, {"prefill_chunk_tiles": 1, "decode_chunk_pages": 2}])

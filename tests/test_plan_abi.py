@@ -212,12 +212,14 @@ def test_host_only_plan_cannot_run(lib):
 
 
 def test_plan_metadata_semantics(lib):
-    """The decode script's batch splits into 2 x 512-key chunks per request
-    on 148 SMs (one wave of 256 items); the mixed batch keeps its long
-    prefill unsplit."""
+    """The decode script's batch runs unsplit on 148 SMs (128 items: one
+    wave that covers most SMs) and in splits of 256 keys on 256 SMs; the
+    mixed batch keeps its long prefill unsplit."""
     w = workloads.decode()
     h = plan_ref.decode_header(_lib_blob(w, num_sms=148))
-    assert (h["n_dec"], h["n_pre"], h["n_merge"], h["dec_chunk_pages"]) == (256, 0, 128, 32)
+    assert (h["n_dec"], h["n_pre"], h["n_merge"], h["dec_chunk_pages"]) == (128, 0, 0, 128)
+    h = plan_ref.decode_header(_lib_blob(w, num_sms=256))
+    assert (h["n_dec"], h["n_pre"], h["n_merge"], h["dec_chunk_pages"]) == (512, 0, 128, 16)
     w = workloads.mixed(num_decode=8, prefill_len=8192, kv_lo=512, kv_hi=8192)
     blob = _lib_blob(w, num_sms=148)
     dec, pre, mer = plan_ref.items(blob)
