@@ -194,6 +194,7 @@ KParams make_params(const RunArgs& a) {
   k.num_pages = hp.num_pages;
   k.scale_log2 = float(1.4426950408889634 / std::sqrt(double(hp.D)));
   k.wait_limit = hp.wait_limit_cycles > 0 ? (long long)hp.wait_limit_cycles : PA_WAIT_LIMIT_CYCLES;
+  k.stall = hp.wait_limit_cycles > 0 ? 1 : 0;
   return k;
 }
 

@@ -37,6 +37,8 @@ struct KParams {
   int32_t hnd;              // cache layout: 0 NHD [P, 2, ps, Hkv, D], 1 HND [P, 2, Hkv, ps, D]
   float scale_log2;         // log2(e) / sqrt(D)
   long long wait_limit;     // clock cycles a pipeline wait may poll before it gives up
+  int32_t stall;            // test hook: 1 = one thread of every CTA first waits on a barrier
+                            // that nothing completes, so that its wait runs out (with a short limit)
 };
 
 // ---------------------------------------------------------------------------

@@ -65,7 +65,8 @@ struct DecCfg {
   static constexpr int OFF_A = OFF_P + kDecPairs * kDecTile * 8 * 8;  // O rescale factor per (pair, head)
   static constexpr int OFF_BAR = OFF_A + kDecPairs * 8 * 4;
   static constexpr int BAR_BYTES = (2 * kDecStages + 2 * kDecPairs) * 8 + 8;  // + abort flag
-  static constexpr int SMEM = OFF_BAR + ((BAR_BYTES + 127) / 128) * 128 + 1024;  // + alignment slack
+  static constexpr int OFF_NEVER = OFF_BAR + BAR_BYTES;  // test hook: a barrier nothing completes
+  static constexpr int SMEM = OFF_BAR + ((BAR_BYTES + 8 + 127) / 128) * 128 + 1024;  // + alignment slack
 };
 
 // Byte offset of 16-byte chunk c (of the row's D/8) of key row t in a stage
@@ -200,6 +201,7 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
   uint64_t* pfull = empty + kDecStages;  // [pairs] QK -> PV
   uint64_t* pempty = pfull + kDecPairs;  // [pairs] PV -> QK
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(pempty + kDecPairs);
+  uint64_t* never = reinterpret_cast<uint64_t*>(smem + C::OFF_NEVER);
   float2* qs2 = reinterpret_cast<float2*>(smem + C::OFF_Q);  // [G][D/2]
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -217,6 +219,7 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
       mbar_init(&pfull[i], 1);
       mbar_init(&pempty[i], 1);
     }
+    mbar_init(never, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -228,6 +231,7 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
   }
   __syncthreads();
 
+  if (p.stall && warp == 0) mbar_wait(never, 0, abort_flag, p.status, p.wait_limit);  // test hook
   if (warp == 2 * kDecPairs) {
     decode_produce<T, D>(kv_map, p, it, rq, smem, full, empty, abort_flag, use_tma, nstage, lane);
     asm volatile("bar.arrive 1, %0;" ::"n"(kDecThreads) : "memory");
@@ -516,6 +520,7 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
   uint64_t* empty = full + kDecStages;
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(empty + kDecStages);
+  uint64_t* never = reinterpret_cast<uint64_t*>(smem + C::OFF_NEVER);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const DecItem it = p.dec[item0 + blockIdx.x];
@@ -528,6 +533,7 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
       mbar_init(&full[i], use_tma ? kDmProds : 32);
       mbar_init(&empty[i], 4);
     }
+    mbar_init(never, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -545,6 +551,7 @@ __global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
     return;
   }
 
+  if (p.stall && warp == 0) mbar_wait(never, 0, abort_flag, p.status, p.wait_limit);  // test hook
   const int rg = warp % RGN, kq = warp / RGN;
   const int g = lane >> 2, t = lane & 3;    // fragment row and column pair
   const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix and row this lane addresses

@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
   uint64_t* fin = o_done + 2;           // all MMAs retired (teardown)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
+  uint64_t* never = bars + 25;          // test hook: a barrier nothing completes
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PreItem it = p.pre[blockIdx.x];
@@ -205,6 +206,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       mbar_init(&o_done[i], 1);
     }
     mbar_init(fin, 1);
+    mbar_init(never, 1);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -363,7 +365,8 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       // tile A's P_lo of the first key tile may live in K slot 0: then that
       // slot is released only once PV_A(0) has read it
       const bool plo_in_k = lo_split0 && (C::OFF_PLO_A == C::OFF_K);
-      bool ok = spin_wait(q_full, 0, abort_flag, p.status, p.wait_limit);
+      bool ok = p.stall ? spin_wait(never, 0, abort_flag, p.status, p.wait_limit) : true;
+      if (ok) ok = spin_wait(q_full, 0, abort_flag, p.status, p.wait_limit);
       if (ok) ok = spin_wait(&full_k[0], 0, abort_flag, p.status, p.wait_limit);
       if (ok) {
         tc_fence_after();

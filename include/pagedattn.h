@@ -91,9 +91,11 @@ typedef struct {
                                   takes 1 only                                      */
   int32_t wait_limit_cycles;   /* test hook: > 0 bounds every in-kernel pipeline wait
                                   at that many SM clock cycles instead of about 2 s,
-                                  so a test can make the waits give up (the run then
-                                  reports PA_DEV_TIMEOUT through device_status and
-                                  leaves out / lse undefined); 0 = the default      */
+                                  and makes one thread of every CTA first wait on a
+                                  barrier that nothing completes, so the waits give
+                                  up (the run then reports PA_DEV_TIMEOUT through
+                                  device_status and leaves out / lse undefined);
+                                  0 = the default                                   */
   int32_t reserved[1];         /* must be 0                                          */
 } pagedattn_options;
 

@@ -465,12 +465,13 @@ def test_cascade_shared_prefix_decode(cuda_cores):
     ("tiny", {"force_cp_async": True, "force_prefill": True}),
     ("decode", {"decode_chunk_pages": 64}), ("decode", {"decode_cuda_cores": True, "decode_chunk_pages": 64})])
 def test_wait_limit_gives_up_then_normal_run(name, opts):
-    """Every in-kernel pipeline wait is bounded.  With the bound cut to one
-    clock cycle (the wait_limit_cycles test hook) the first wait that finds
-    its data not yet there gives up: the CTA drains the copies and MMAs it
-    has in flight, releases its TMEM and returns, and the run reports
-    PA_DEV_TIMEOUT through the device status word.  A normal run on the same
-    workspace afterwards matches the oracle."""
+    """Every in-kernel pipeline wait is bounded.  The wait_limit_cycles test
+    hook cuts the bound to one clock cycle and has one thread of every CTA
+    wait on a barrier that nothing completes (a flag nobody sets): that wait
+    gives up, the CTA drains the copies and MMAs it has in flight, releases
+    its TMEM and returns, and the run reports PA_DEV_TIMEOUT through the
+    device status word.  A normal run on the same workspace afterwards
+    matches the oracle."""
     w = workloads.tiny() if name == "tiny" else workloads.decode(batch_size=16, seq_len=1000)
     ws = torch.empty(pa.DEFAULT_WORKSPACE_BYTES, dtype=torch.uint8, device="cuda")
     q, kv = w.q.cuda(), w.kv_cache.cuda()
