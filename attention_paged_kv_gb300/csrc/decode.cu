@@ -459,8 +459,10 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
 //              become the A fragment of P V directly; ldmatrix.trans feeds V.
 //              O stays in registers; the key subsets are combined at the end.
 // Row classes (template RC): up to 8 and up to 16 rows (RGN 1; fragment rows
-// past R see no keys), 32 (RGN 2) and 64 (RGN 4); the first two run the same
-// code and differ only in how the planner groups items.  Each row's keys end at its own causal limit.  For requests with
+// past R see no keys) and 32 (RGN 2); the first two run the same code and
+// differ only in how the planner groups items.  (64 rows, RGN 4, is never
+// planned: there the warp-level MMA bound the kernel at 43 % of HBM, and the
+// tcgen05 prefill kernel is faster.)  Each row's keys end at its own causal limit.  For requests with
 // fewer than 128 keys P is split into hi + lo halves (two MMAs), as in the
 // prefill kernel, so rows that see few keys keep P's rounding out of the
 // output.
@@ -499,14 +501,15 @@ constexpr int kDmThreads = 32 * (4 + kDmProds);    // 4 MMA warps + producer(s)
 
 template <int RC>
 struct RowClass {
-  static constexpr int RGN = RC <= 1 ? 1 : (RC == 2 ? 2 : 4);  // row groups of 16
+  static_assert(RC >= 0 && RC <= 2, "row classes of up to 32 rows");
+  static constexpr int RGN = RC <= 1 ? 1 : 2;                  // row groups of 16
   static constexpr int KS = 4 / RGN;                           // key subsets (warps per row group)
   static constexpr int KW = kDecTile / KS;                     // keys per warp per stage
   static constexpr int NKB = KW / 16;                          // 16-key blocks per warp
 };
 
 template <typename T, int D, int RC>
-__global__ void __launch_bounds__(kDmThreads, RC == 3 ? 1 : 2)
+__global__ void __launch_bounds__(kDmThreads, 2)
     decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p, const int use_tma,
                       const int item0) {
   using C = DecCfg<D>;
@@ -909,7 +912,7 @@ cudaError_t launch_decode_d(const RunArgs& a, const CUtensorMap* map, const KPar
         case 0: e = launch_mma<T, D, 0>(a, m, kp, use_tma, item0, n); break;
         case 1: e = launch_mma<T, D, 1>(a, m, kp, use_tma, item0, n); break;
         case 2: e = launch_mma<T, D, 2>(a, m, kp, use_tma, item0, n); break;
-        default: e = launch_mma<T, D, 3>(a, m, kp, use_tma, item0, n); break;
+        default: e = cudaErrorInvalidValue; break;  // 64-row items go to the prefill kernel
       }
       if (e != cudaSuccess) return e;
       item0 += n;

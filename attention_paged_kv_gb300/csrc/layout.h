@@ -22,7 +22,7 @@ enum HdrIdx : int {
 constexpr int32_t kMagic = 0x50414731;
 constexpr int32_t kVersion = 5;
 constexpr int kDecClasses = 4;
-constexpr int kDecMaxRows = 64;  // packed (token, head) rows of a small-query item
+constexpr int kDecMaxRows = 32;  // packed (token, head) rows of a small-query item
 constexpr int kQRows = 128;   // packed query rows per prefill MMA tile
 constexpr int kItemRows = 256;  // packed query rows per prefill work item (two tiles)
 constexpr int kKvTile = 128;  // keys per prefill key tile

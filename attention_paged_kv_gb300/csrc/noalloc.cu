@@ -64,7 +64,7 @@ extern "C" pagedattn_status pagedattn_run_decode_noalloc(pagedattn_plan_t plan, 
   if (hp.n_pre > 0)
     return set_err(PA_ERR_UNSUPPORTED,
                    "pagedattn_run_decode_noalloc runs decode batches only: every request needs qo_len 0 or "
-                   "qo_len * G <= 64 with G = num_qo_heads / num_kv_heads in {1, 2, 4, 8, 16}, without "
+                   "qo_len * G <= 32 with G = num_qo_heads / num_kv_heads in {1, 2, 4, 8, 16}, without "
                    "force_prefill (qo_len 1 and G <= 8 with decode_cuda_cores or at head_dim 256)");
   if (hp.total_bytes > kNoallocScratchBytes)
     return set_err(PA_ERR_WORKSPACE_TOO_SMALL,

@@ -10,8 +10,10 @@
 //     last, 1 <= last <= page_size as the timing script's comment requires).
 //  2. Small-query requests go to the decode kernels: with group size
 //     G = Hq/Hkv in {1, 2, 4, 8, 16}, a request whose R_b = qo_b * G packed
-//     (token, head) rows number at most 64 (one decoded token, or a few
-//     speculative ones) and, when qo_b > 1, that has more keys than one
+//     (token, head) rows number at most 32 (one decoded token, or a few
+//     speculative ones; at 64 rows the warp-level MMA, not HBM, bounds the
+//     small-query kernel, and the tcgen05 prefill kernel ran 64 requests of
+//     8 tokens at G 8 in 0.251 ms against 0.401 ms) and, when qo_b > 1, that has more keys than one
 //     prefill key tile (kv_b > 128; a shorter one costs the prefill kernel
 //     a single key tile), unless force_prefill.  With decode_cuda_cores, or
 //     at head_dim 256 (where the warp-MMA kernel's fragments would not fit
@@ -19,8 +21,8 @@
 //     kernel's shapes).  Every other request with rows -> tensor-core
 //     prefill.  The decode items run on the CUDA-core kernel in those two
 //     cases, or when G <= 2 and every small-query request has qo_b == 1;
-//     else on the warp-MMA kernel.  Row class of an item: R_b <= 8, 16, 32
-//     or 64.
+//     else on the warp-MMA kernel.  Row class of an item: R_b <= 8, 16 or
+//     32 (a fourth class, 64 rows, is never planned).
 //  3. Decode split ("kv-parallelism" / split-k in the same issue): chunk c0 =
 //     clamp(ceil(P_dec / (4 * SMs)), 256 keys, 2048 keys) in whole pages,
 //     P_dec = sum of decode pages x Hkv.  With N(c) = sum over (request,
@@ -40,9 +42,14 @@
 //     do the G heads).  Items of one 128-row tile instead (two CTAs then
 //     share an SM) at head_dim 256 (two tiles' accumulators would not fit
 //     in tensor memory), with prefill_q_tiles = 1, or when most two-tile
-//     items would run only their first tile: with n1 = sum over prefill
-//     requests (and cascade prefixes) of ceil(qo_b / (128/G)) and n2 the
-//     same at 256/G, when 2 * n1 <= 3 * n2.  An item needs keys [0, kv_b - qo_b + t0 + n) under
+//     items would run only their first tile over short key ranges: with
+//     n1 = sum over prefill requests (and cascade prefixes) of
+//     ceil(qo_b / (128/G)), n2 the same at 256/G and w1 = sum of
+//     ceil(qo_b / (128/G)) x ceil(kv_b / 128), when 2 * n1 <= 3 * n2 and
+//     w1 <= 8 * n1 (the two-tile CTA has a producer warp for K and one for
+//     V, the one-tile CTA one for both, which limits it on long key ranges:
+//     64 requests x 8 tokens over 512..8192 keys ran 0.279 ms on one-tile
+//     items, 0.251 ms on two-tile items).  An item needs keys [0, kv_b - qo_b + t0 + n) under
 //     the bottom-right causal mask; key tiles past that are never visited
 //     (the "skips the fully masked out tails" of the llama.cpp discussion
 //     "Pad for prefill stage?").  Split when the
@@ -253,17 +260,18 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
     pre_tiles = 1;
   } else if (in.prefill_q_tiles > 0) {
     pre_tiles = in.prefill_q_tiles;
-  } else {  // one tile when most two-tile items would run only their first tile
-    int64_t n1 = 0, n2 = 0;
-    auto count = [&](int64_t qo) {
+  } else {  // one tile when most two-tile items would run only their first tile, over short key ranges
+    int64_t n1 = 0, n2 = 0, w1 = 0;
+    auto count = [&](int64_t qo, int64_t kv) {
       n1 += cdiv(qo, kQRows / G);
       n2 += cdiv(qo, kItemRows / G);
+      w1 += cdiv(qo, kQRows / G) * cdiv(kv, kKvTile);
     };
     for (int b = 0; b < B; ++b)
-      if (!is_dec[b] && req[b].qo > 0) count(req[b].qo);
+      if (!is_dec[b] && req[b].qo > 0) count(req[b].qo, req[b].kv);
     for (const Grp& g : grp)
-      if (g.np > 0 && g.T > 0) count(g.T);
-    if (2 * n1 <= 3 * n2) pre_tiles = 1;
+      if (g.np > 0 && g.T > 0) count(g.T, int64_t(g.np) * ps);
+    if (2 * n1 <= 3 * n2 && w1 <= 8 * n1) pre_tiles = 1;
   }
   const int32_t tq = pre_tiles * kQRows / G;
   struct Tile { int32_t b, t0, n; int64_t e; };

@@ -97,7 +97,7 @@ def unique_slots(w, reqs) -> int:
 def accounting(w):
     """Algorithmic flops and bytes of the step, split into the prefill part
     (requests the planner gives to the tcgen05 prefill kernel) and the decode
-    part (single-token and small-query requests: qo_len * G <= 64 packed rows
+    part (single-token and small-query requests: qo_len * G <= 32 packed rows
     at a group size G of 1, 2, 4, 8 or 16, and more than 128 keys when
     qo_len > 1; at head_dim 256 single-token requests at G <= 8 only -- the
     planner's rule)."""
@@ -106,7 +106,7 @@ def accounting(w):
     npg = np.diff(w.kv_page_indptr).astype(np.int64)
     D, Hq, Hkv, e = w.head_dim, w.num_qo_heads, w.num_kv_heads, 2
     G = Hq // Hkv
-    small = (qo >= 1) & (qo * G <= 64) & (G in (1, 2, 4, 8, 16)) & ((qo == 1) | (kv > 128))
+    small = (qo >= 1) & (qo * G <= 32) & (G in (1, 2, 4, 8, 16)) & ((qo == 1) | (kv > 128))
     if D == 256:
         small &= (qo == 1) & (G <= 8)
     res = {}
@@ -433,6 +433,7 @@ def main():
     ap.add_argument("--decode-chunk-pages", type=int, default=0, help="planner override (0: the plan's rule)")
     ap.add_argument("--prefill-chunk-tiles", type=int, default=0, help="planner override (0: the plan's rule)")
     ap.add_argument("--prefill-q-tiles", type=int, default=0, help="planner override (0: the plan's rule)")
+    ap.add_argument("--force-prefill", action="store_true", help="planner override: every request on the prefill kernel")
     ap.add_argument("--workload", default="mixed", choices=list(WORKLOADS),
                     help="mixed is the benchmark; the others exist for profiling captures")
     args = ap.parse_args()
@@ -486,7 +487,7 @@ def main():
     stream = torch.cuda.current_stream(dev)
     sh = stream.cuda_stream
     popts = {"decode_chunk_pages": args.decode_chunk_pages, "prefill_chunk_tiles": args.prefill_chunk_tiles,
-             "prefill_q_tiles": args.prefill_q_tiles}
+             "prefill_q_tiles": args.prefill_q_tiles, "force_prefill": args.force_prefill}
     pargs = w.plan_args()
     if args.workload in CASCADE:
         groups, pargs = workloads.split_prefix(w, *CASCADE[args.workload])
@@ -652,7 +653,7 @@ WORKLOAD_DESC = {
     "decode_g2": "the decode script's shape re-headed to Hq 2 / Hkv 1 (CUDA-core decode kernel), 512 requests "
                  "x 1024 keys, fp16",
     "decode_mixed64": "64 decodes with kv_len U[512,8192], Hq 64 / Hkv 8, head_dim 128, page_size 16, bf16",
-    "specdec8": "64 requests x 8 query tokens (64 packed rows a kv head), kv_len U[512,8192], Hq 64 / Hkv 8, "
+    "specdec8": "64 requests x 8 query tokens (64 packed rows a kv head: prefill kernel), kv_len U[512,8192], Hq 64 / Hkv 8, "
                 "head_dim 128, page_size 16, bf16",
 }
 

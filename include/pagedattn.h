@@ -241,7 +241,7 @@ PAGEDATTN_API pagedattn_status pagedattn_workspace_size_cascade(const pagedattn_
  * stream   the stream every kernel is queued on.
  *
  * Launches the prefill kernel (tcgen05 / TMEM), the small-query kernels
- * (decode and requests of qo_len * G <= 64 rows: warp-level MMA, one launch
+ * (decode and requests of qo_len * G <= 32 rows: warp-level MMA, one launch
  * per row class, or the CUDA-core decode kernel) and, when some request was
  * split, the merge kernel, in that order on `stream`.  Allocates nothing and does not synchronise the host.  In-kernel
  * waits are bounded; a wait that gives up sets PA_DEV_TIMEOUT in the device
@@ -311,7 +311,7 @@ PAGEDATTN_API pagedattn_status pagedattn_debug_gather(pagedattn_plan_t plan, int
  * lse are as for pagedattn_run.
  *
  * The batch must have no prefill items (every request has qo_len 0 or
- * qo_len * G <= 64 with the group size G = num_qo_heads / num_kv_heads in
+ * qo_len * G <= 32 with the group size G = num_qo_heads / num_kv_heads in
  * {1, 2, 4, 8, 16}, and force_prefill is off; with decode_cuda_cores or at
  * head_dim 256, qo_len <= 1 and G <= 8): PA_ERR_UNSUPPORTED otherwise.  A plan whose metadata and partial
  * states exceed 16 MiB returns PA_ERR_WORKSPACE_TOO_SMALL (plan with a larger

@@ -14,14 +14,14 @@ Rules (the planner is deterministic; nothing depends on timing):
    (see ``oracle.attention.kv_len_of``), page_start_b.
 2. Small-query requests go to the decode kernels: G = Hq/Hkv is one of
    1, 2, 4, 8, 16, the request's R_b = qo_b * G packed (token, head) rows
-   number at most 64, a request with qo_b > 1 has kv_b > 128 (more keys
+   number at most 32, a request with qo_b > 1 has kv_b > 128 (more keys
    than one prefill key tile), and ``force_prefill`` is off.  With
    ``decode_cuda_cores``, or at head_dim 256, only qo_b == 1 at G <= 8
    qualifies.  Every other request with qo_b >= 1 goes to the tensor-core
    prefill kernel.  The decode items run on CUDA cores (header word 29 = 1)
    in those two cases, or when G <= 2 and no small-query request has
    qo_b > 1; else on the warp-MMA kernel (0).  An item's row class is
-   0, 1, 2, 3 for R_b <= 8, 16, 32, 64.
+   0, 1, 2 for R_b <= 8, 16, 32 (class 3, 64 rows, is never planned).
 3. Decode split ("kv-parallelism", the split-k of the same issue): with
    P_dec = sum over decode requests of pages_b * Hkv and
    target = 4 * num_sms, the first choice is
@@ -38,9 +38,11 @@ Rules (the planner is deterministic; nothing depends on timing):
 4. Prefill items: 256 packed rows = (256 / G) query tokens x G heads (two
    128-row tiles); 128 packed rows (one tile) at head_dim 256, with
    ``prefill_q_tiles`` = 1, or when n1 = sum over prefill requests (and
-   cascade prefixes, of T_g tokens) of ceil(qo_b / (128 / G)) and n2, the
-   same at 256 / G, satisfy 2 * n1 <= 3 * n2 (most two-tile items would run
-   only their first tile).  Item [t0, t0 + n) of request b needs keys [0, e) with
+   cascade prefixes, of T_g tokens over np_g * page_size keys) of
+   ceil(qo_b / (128 / G)), n2, the same at 256 / G, and w1 = sum of
+   ceil(qo_b / (128 / G)) * ceil(kv_b / 128) satisfy 2 * n1 <= 3 * n2
+   (most two-tile items would run only their first tile) and w1 <= 8 * n1
+   (their key ranges are short).  Item [t0, t0 + n) of request b needs keys [0, e) with
    e = kv_b - qo_b + t0 + n (causal) or kv_b; that is ceil(e / 128) key
    tiles of 128.  With W = the
    sum of key tiles over all (tile, kv head) items and target = 2 * num_sms,
@@ -95,7 +97,7 @@ DEC_WAVE_PER_SM = 2   # resident small-query CTAs per SM
 PRE_ITEMS_PER_SM = 2
 PRE_MIN_CHUNK_TILES = 8
 DECODE_GROUPS = (1, 2, 4, 8, 16)
-DEC_MAX_ROWS = 64
+DEC_MAX_ROWS = 32
 DEC_CLASS_ROWS = (8, 16, 32, 64)
 
 FP16, BF16 = 0, 1
@@ -219,11 +221,12 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
     elif prefill_q_tiles:
         pre_tiles = int(prefill_q_tiles)
     else:   # one tile when most two-tile items would run only their first tile
-        qos = [l[0] for l, d in zip(lens, is_dec) if not d and l[0] > 0]
-        qos += [g[2] for g in groups if g[3] > 0 and g[2] > 0]
-        n1 = sum(_cdiv(q, Q_ROWS // G) for q in qos)
-        n2 = sum(_cdiv(q, ITEM_ROWS // G) for q in qos)
-        pre_tiles = 1 if 2 * n1 <= 3 * n2 else 2
+        qk = [(l[0], l[1]) for l, d in zip(lens, is_dec) if not d and l[0] > 0]
+        qk += [(g[2], g[3] * ps) for g in groups if g[3] > 0 and g[2] > 0]
+        n1 = sum(_cdiv(q, Q_ROWS // G) for q, _ in qk)
+        n2 = sum(_cdiv(q, ITEM_ROWS // G) for q, _ in qk)
+        w1 = sum(_cdiv(q, Q_ROWS // G) * _cdiv(k, KV_TILE) for q, k in qk)
+        pre_tiles = 1 if (2 * n1 <= 3 * n2 and w1 <= 8 * n1) else 2
     tq = pre_tiles * Q_ROWS // G
 
     def tiles_of(b):

@@ -398,7 +398,7 @@ def test_plan_ref_covers_every_pair_once(wname, sms, kw):
     lens = A.request_lengths(w.qo_indptr, w.kv_page_indptr, w.kv_last_page_len, w.page_size)
     for (b, hk, t0, t1, pr, *_r) in dec:
         qo, kv = lens[b][0], lens[b][1]
-        assert qo * G <= 64
+        assert qo * G <= 32
         for i in range(qo):
             vis = kv - qo + i + 1 if w.causal else kv
             row = int(w.qo_indptr[b]) + i

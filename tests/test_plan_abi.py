@@ -84,7 +84,7 @@ def make(name):
                                      dtype=torch.bfloat16, seed=5)
     if name == "random_nc":
         return workloads.make_custom("r", [3, 1, 200], [2, 7, 40], 8, 8, 64, 2, causal=False, seed=6)
-    if name == "smallq":  # G 8: 32, 32, 16, 8 and 64 packed rows, and a 9-token prefill
+    if name == "smallq":  # G 8: 32, 32, 16 and 8 packed rows, 64 rows and a 9-token prefill
         return workloads.make_custom("sq", [4, 4, 2, 1, 8, 9], [300, 40, 900, 70, 500, 9], 16, 2, 128, 16,
                                      dtype=torch.bfloat16, seed=11)
     if name == "smallq_g16":
@@ -229,7 +229,7 @@ def test_plan_metadata_semantics(lib):
 
 
 def test_plan_small_query_semantics(lib):
-    """Requests of a few query tokens (qo_len * G <= 64 packed rows) become
+    """Requests of a few query tokens (qo_len * G <= 32 packed rows) become
     small-query items of the decode kernels, grouped by row class; their
     split groups merge per (token, kv head) with a stride of qo_len * G."""
     w = workloads.mixed(num_decode=24, prefill_len=0, kv_lo=200, kv_hi=3000, decode_qo=4)
