@@ -72,6 +72,29 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
 
+// Programmatic dependent launch.  Every kernel of a run is launched with
+// programmatic stream serialization, so a kernel may start while the kernel
+// before it on the stream is still running.  pdl_wait() returns once that
+// kernel has completed and its writes are visible; each kernel calls it
+// after its prologue (barrier set-up, work-item and page-id reads from the
+// plan's metadata, which no kernel writes) and before it reads q, the cache
+// or partial states, or writes anything.  pdl_launch() lets the next
+// kernel's CTAs be scheduled once every CTA of this grid has issued it (or
+// exited); the attention kernels issue it when their main loop is done, so
+// the next kernel's prologue overlaps only their epilogue (issued at the
+// start, it measured slower on one-wave decode batches).  Launched without
+// the attribute, the wait returns at once.  PA_NO_PDL builds without it.
+__device__ __forceinline__ void pdl_wait() {
+#ifndef PA_NO_PDL
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+__device__ __forceinline__ void pdl_launch() {
+#ifndef PA_NO_PDL
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
 __device__ __forceinline__ void mbar_init_fence() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -54,17 +54,17 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-template <int D>
+template <int D, int NST = kDecStages>
 struct DecCfg {
   static constexpr int NKB = D / 64;                  // 128-byte column blocks of a row
   static constexpr int BLK = kDecTile * 128;          // 64 rows x 128 bytes
   static constexpr int STAGE_K = NKB * BLK;
   static constexpr int STAGE = 2 * STAGE_K;           // K then V
-  static constexpr int OFF_Q = kDecStages * STAGE;    // q: up to 8 heads x D fp32
+  static constexpr int OFF_Q = NST * STAGE;          // q: up to 8 heads x D fp32
   static constexpr int OFF_P = OFF_Q + 8 * D * 4;     // P as (p, p) pairs: per pair 64 keys x 8 heads
   static constexpr int OFF_A = OFF_P + kDecPairs * kDecTile * 8 * 8;  // O rescale factor per (pair, head)
   static constexpr int OFF_BAR = OFF_A + kDecPairs * 8 * 4;
-  static constexpr int BAR_BYTES = (2 * kDecStages + 2 * kDecPairs) * 8 + 8;  // + abort flag
+  static constexpr int BAR_BYTES = (2 * NST + 2 * kDecPairs) * 8 + 8;  // + abort flag
   static constexpr int OFF_NEVER = OFF_BAR + BAR_BYTES;  // test hook: a barrier nothing completes
   static constexpr int SMEM = OFF_BAR + ((BAR_BYTES + 8 + 127) / 128) * 128 + 1024;  // + alignment slack
 };
@@ -78,18 +78,18 @@ __device__ __forceinline__ uint32_t sw_off(int t, int c) {
 }
 
 // Producer warp of the decode kernels: streams the item's keys in 64-key
-// stages (K then V, 128-byte-swizzled rows) into kDecStages buffers, by TMA
+// stages (K then V, 128-byte-swizzled rows) into NST buffers, by TMA
 // through the page table or, for pages of fewer than 8 slots, by cp.async.
 // With TMA it copies the halves [h0, h1) of each stage (0 = K, 1 = V), so two
 // producer warps can share a stage's copies; each then arrives on the
 // stage's full barrier with its own byte count.  On return every copy it
 // issued has landed (or its wait gave up).
-template <typename T, int D>
+template <typename T, int D, int NST = kDecStages>
 __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const KParams& p, const DecItem& it,
                                                const ReqEntry& rq, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                                volatile int32_t* abort_flag, int use_tma, int nstage, int lane,
                                                int h0 = 0, int h1 = 2) {
-  using C = DecCfg<D>;
+  using C = DecCfg<D, NST>;
   constexpr int NKB = C::NKB;
   constexpr int NCH = D / 8;
     if (use_tma && lane == 0) tma_prefetch_desc(&kv_map);
@@ -108,6 +108,7 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
       return lane < nb ? __ldg(p.pages + rq.page_start + ((s0j + lane * BR) >> p.ps_shift)) : 0;
     };
     int pids[3] = {stage_pid(0), stage_pid(1), stage_pid(2)};
+    pdl_wait();  // the cache may come from the previous kernel on the stream
     int issued = 0;
     bool ok = true;
     for (int j0 = 0; ok && j0 < nstage; j0 += 3) {
@@ -115,11 +116,11 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
      for (int u = 0; u < 3; ++u) {
       const int j = j0 + u;
       if (!ok || j >= nstage) break;
-      const int st = j % kDecStages;
+      const int st = j % NST;
       int pid = pids[u];
       pids[u] = stage_pid(j + 3);
-      if (j >= kDecStages) {
-        if (lane == 0) ok = mbar_wait(&empty[st], ((j / kDecStages) - 1) & 1, abort_flag, p.status, p.wait_limit);
+      if (j >= NST) {
+        if (lane == 0) ok = mbar_wait(&empty[st], ((j / NST) - 1) & 1, abort_flag, p.status, p.wait_limit);
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
       }
@@ -176,20 +177,20 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
      }
     }
     if (use_tma && lane == 0) {
-      for (int j = max(0, issued - kDecStages); j < issued; ++j) {
-        const uint32_t a = smem_u32(&full[j % kDecStages]);
+      for (int j = max(0, issued - NST); j < issued; ++j) {
+        const uint32_t a = smem_u32(&full[j % NST]);
         const long long t0 = clock64();
-        while (!mbar_try_wait(a, (j / kDecStages) & 1))
+        while (!mbar_try_wait(a, (j / NST) & 1))
           if (clock64() - t0 > PA_WAIT_LIMIT_CYCLES) break;
       }
     }
     __syncwarp();
 }
 
-template <typename T, int D, int G>
-__global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
+template <typename T, int D, int G, int NST>
+__global__ void __launch_bounds__(kDecThreads, (NST <= 3 ? 2 : 1))
     decode_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p, const int use_tma) {
-  using C = DecCfg<D>;
+  using C = DecCfg<D, NST>;
   constexpr int NKB = C::NKB;
   constexpr int NCH = D / 8;       // 16-byte chunks per row
   constexpr int LPT = D / 8;       // PV lanes per key
@@ -197,8 +198,8 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* empty = full + kDecStages;
-  uint64_t* pfull = empty + kDecStages;  // [pairs] QK -> PV
+  uint64_t* empty = full + NST;
+  uint64_t* pfull = empty + NST;  // [pairs] QK -> PV
   uint64_t* pempty = pfull + kDecPairs;  // [pairs] PV -> QK
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(pempty + kDecPairs);
   uint64_t* never = reinterpret_cast<uint64_t*>(smem + C::OFF_NEVER);
@@ -211,7 +212,7 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
   const int64_t qrow0 = int64_t(rq.qo_start) * p.Hq + int64_t(it.kv_head) * G;
 
   if (tid == 0) {
-    for (int i = 0; i < kDecStages; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], use_tma ? 1 : 32);
       mbar_init(&empty[i], 2);
     }
@@ -223,6 +224,7 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
     *abort_flag = 0;
     mbar_init_fence();
   }
+  pdl_wait();  // q may come from the previous kernel on the stream
   // q for the G heads, pre-scaled into log2 units, as fp32 column pairs
   for (int idx = tid; idx < G * D / 2; idx += kDecThreads) {
     const int g = idx / (D / 2), c2 = idx % (D / 2);
@@ -233,7 +235,7 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
 
   if (p.stall && warp == 0) mbar_wait(never, 0, abort_flag, p.status, p.wait_limit);  // test hook
   if (warp == 2 * kDecPairs) {
-    decode_produce<T, D>(kv_map, p, it, rq, smem, full, empty, abort_flag, use_tma, nstage, lane);
+    decode_produce<T, D, NST>(kv_map, p, it, rq, smem, full, empty, abort_flag, use_tma, nstage, lane);
     asm volatile("bar.arrive 1, %0;" ::"n"(kDecThreads) : "memory");
     return;
   }
@@ -255,8 +257,8 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
     }
     const int t0 = lane, t1 = lane + 32;
     for (int k = 0, j = pair; j < nstage; ++k, j += kDecPairs) {
-      const int st = j % kDecStages;
-      bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status, p.wait_limit);
+      const int st = j % NST;
+      bool ok = mbar_wait(&full[st], (j / NST) & 1, abort_flag, p.status, p.wait_limit);
       if (!__all_sync(0xffffffffu, ok)) break;
       const int nval = min(kDecTile, it.tok1 - (it.tok0 + j * kDecTile));
       const uint8_t* kst = smem + st * C::STAGE;
@@ -341,8 +343,8 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
 #pragma unroll
       for (int i = 0; i < 4; ++i) o2[g][i] = make_float2(0.f, 0.f);
     for (int k = 0, j = pair; j < nstage; ++k, j += kDecPairs) {
-      const int st = j % kDecStages;
-      bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status, p.wait_limit);
+      const int st = j % NST;
+      bool ok = mbar_wait(&full[st], (j / NST) & 1, abort_flag, p.status, p.wait_limit);
       if (ok) ok = mbar_wait(&pfull[pair], k & 1, abort_flag, p.status, p.wait_limit);
       if (!__all_sync(0xffffffffu, ok)) break;
       const int nval = min(kDecTile, it.tok1 - (it.tok0 + j * kDecTile));
@@ -403,6 +405,7 @@ __global__ void __launch_bounds__(kDecThreads, (kDecStages <= 3 ? 2 : 1))
     }
   }
 
+  pdl_launch();
   // ---------------------------------------------------------------- combine the pairs
   asm volatile("bar.sync 2, %0;" ::"n"(64 * kDecPairs) : "memory");
   if (*abort_flag) return;
@@ -508,11 +511,11 @@ struct RowClass {
   static constexpr int NKB = KW / 16;                          // 16-key blocks per warp
 };
 
-template <typename T, int D, int RC>
-__global__ void __launch_bounds__(kDmThreads, 2)
+template <typename T, int D, int RC, int NST>
+__global__ void __launch_bounds__(kDmThreads, NST <= 3 ? 2 : 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p, const int use_tma,
                       const int item0) {
-  using C = DecCfg<D>;
+  using C = DecCfg<D, NST>;
   using RCl = RowClass<RC>;
   constexpr int RGN = RCl::RGN, KS = RCl::KS, KW = RCl::KW, NKB = RCl::NKB;
   constexpr int NA = 4;        // fragment registers per lane: rows lo (0, 1) and hi (2, 3)
@@ -521,8 +524,8 @@ __global__ void __launch_bounds__(kDmThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::OFF_BAR);
-  uint64_t* empty = full + kDecStages;
-  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(empty + kDecStages);
+  uint64_t* empty = full + NST;
+  volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(empty + NST);
   uint64_t* never = reinterpret_cast<uint64_t*>(smem + C::OFF_NEVER);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -532,7 +535,7 @@ __global__ void __launch_bounds__(kDmThreads, 2)
   const int R = rq.qo_len << p.g_shift;  // packed rows: r = token * G + head
 
   if (tid == 0) {
-    for (int i = 0; i < kDecStages; ++i) {
+    for (int i = 0; i < NST; ++i) {
       mbar_init(&full[i], use_tma ? kDmProds : 32);
       mbar_init(&empty[i], 4);
     }
@@ -548,13 +551,14 @@ __global__ void __launch_bounds__(kDmThreads, 2)
     if (warp == 4 || use_tma) {
       const int h0 = (kDmProds == 2 && use_tma && warp == 5) ? 1 : 0;
       const int h1 = (kDmProds == 2 && use_tma && warp == 4) ? 1 : 2;
-      decode_produce<T, D>(kv_map, p, it, rq, smem, full, empty, abort_flag, use_tma, nstage, lane, h0, h1);
+      decode_produce<T, D, NST>(kv_map, p, it, rq, smem, full, empty, abort_flag, use_tma, nstage, lane, h0, h1);
     }
     asm volatile("bar.arrive 1, %0;" ::"n"(kDmThreads) : "memory");
     return;
   }
 
   if (p.stall && warp == 0) mbar_wait(never, 0, abort_flag, p.status, p.wait_limit);  // test hook
+  pdl_wait();  // q may come from the previous kernel on the stream
   const int rg = warp % RGN, kq = warp / RGN;
   const int g = lane >> 2, t = lane & 3;    // fragment row and column pair
   const int mi = lane >> 3, ri = lane & 7;  // ldmatrix: matrix and row this lane addresses
@@ -609,8 +613,8 @@ __global__ void __launch_bounds__(kDmThreads, 2)
   const int kofs = kq * KW;  // this warp's first key in every stage
 
   for (int j = 0; j < nstage; ++j) {
-    const int st = j % kDecStages;
-    const bool ok = mbar_wait(&full[st], (j / kDecStages) & 1, abort_flag, p.status, p.wait_limit);
+    const int st = j % NST;
+    const bool ok = mbar_wait(&full[st], (j / NST) & 1, abort_flag, p.status, p.wait_limit);
     if (!__all_sync(0xffffffffu, ok)) break;
     const int s0 = it.tok0 + j * kDecTile;         // absolute position of the stage's first key
     const int nval = min(kDecTile, it.tok1 - s0);  // keys of the stage inside the item's range
@@ -729,6 +733,7 @@ __global__ void __launch_bounds__(kDmThreads, 2)
     if (lane == 0) mbar_arrive(&empty[st]);
   }
 
+  pdl_launch();
   // ---------------------------------------------------------------- combine the key subsets
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
@@ -815,6 +820,7 @@ __global__ void __launch_bounds__(256) merge_kernel(const KParams p, const int n
   if (gw >= n_rows) return;
   const MergeEntry e = p.merge[gw / p.G];
   const int g = gw % p.G;
+  pdl_wait();  // the partial states come from the attention kernels before it
   float M = -INFINITY;
   for (int s = 0; s < e.nsplit; ++s) M = fmaxf(M, p.part_lse[e.part_row0 + s * e.split_stride + g]);
   const float Mu = (M == -INFINITY) ? 0.f : M;
@@ -860,25 +866,47 @@ __global__ void debug_gather_kernel(const KParams p, const int B, int32_t* page_
   }
 }
 
+// Stages of a decode launch: a launch of at most one CTA per SM streams each
+// item through 192 KB of stages (one CTA per SM); larger launches keep two
+// CTAs of kDecStages stages on an SM.  The bytes in flight per SM set the
+// pace: the decode timing script's 128 items ran 15.8 us with one CTA of 3
+// stages on each of 128 SMs and 14.6 us with 6, while batches of several
+// waves ran 40 % slower with one CTA of 4 stages per SM than with two of 3.
+template <int D>
+constexpr int kDeepStages = (192 * 1024) / DecCfg<D>::STAGE;
+
+template <typename T, int D, int G, int NST>
+cudaError_t launch_cuda_cores_n(const RunArgs& a, const CUtensorMap* map, const KParams& kp, int use_tma) {
+  using C = DecCfg<D, NST>;
+  static std::atomic<uint64_t> attr_set{0};
+  cudaError_t e = set_smem_once(attr_set, reinterpret_cast<const void*>(decode_kernel<T, D, G, NST>), C::SMEM);
+  if (e != cudaSuccess) return e;
+  return launch_pdl(decode_kernel<T, D, G, NST>, unsigned(a.hp->n_dec), unsigned(kDecThreads), size_t(C::SMEM),
+                    a.stream, *map, kp, use_tma);
+}
+
 template <typename T, int D, int G>
 cudaError_t launch_cuda_cores(const RunArgs& a, const CUtensorMap* map, const KParams& kp, int use_tma) {
-  using C = DecCfg<D>;
+  if (a.hp->n_dec <= a.hp->num_sms) return launch_cuda_cores_n<T, D, G, kDeepStages<D>>(a, map, kp, use_tma);
+  return launch_cuda_cores_n<T, D, G, kDecStages>(a, map, kp, use_tma);
+}
+
+template <typename T, int D, int RC, int NST>
+cudaError_t launch_mma_n(const RunArgs& a, const CUtensorMap* map, const KParams& kp, int use_tma, int item0,
+                         int n) {
+  using C = DecCfg<D, NST>;
   static std::atomic<uint64_t> attr_set{0};
-  cudaError_t e = set_smem_once(attr_set, reinterpret_cast<const void*>(decode_kernel<T, D, G>), C::SMEM);
+  cudaError_t e = set_smem_once(attr_set, reinterpret_cast<const void*>(decode_mma_kernel<T, D, RC, NST>), C::SMEM);
   if (e != cudaSuccess) return e;
-  decode_kernel<T, D, G><<<a.hp->n_dec, kDecThreads, C::SMEM, a.stream>>>(*map, kp, use_tma);
-  return cudaGetLastError();
+  return launch_pdl(decode_mma_kernel<T, D, RC, NST>, unsigned(n), unsigned(kDmThreads), size_t(C::SMEM), a.stream,
+                    *map, kp, use_tma, item0);
 }
 
 template <typename T, int D, int RC>
 cudaError_t launch_mma(const RunArgs& a, const CUtensorMap* map, const KParams& kp, int use_tma, int item0,
                        int n) {
-  using C = DecCfg<D>;
-  static std::atomic<uint64_t> attr_set{0};
-  cudaError_t e = set_smem_once(attr_set, reinterpret_cast<const void*>(decode_mma_kernel<T, D, RC>), C::SMEM);
-  if (e != cudaSuccess) return e;
-  decode_mma_kernel<T, D, RC><<<n, kDmThreads, C::SMEM, a.stream>>>(*map, kp, use_tma, item0);
-  return cudaGetLastError();
+  if (n <= a.hp->num_sms) return launch_mma_n<T, D, RC, kDeepStages<D>>(a, map, kp, use_tma, item0, n);
+  return launch_mma_n<T, D, RC, kDecStages>(a, map, kp, use_tma, item0, n);
 }
 
 // The plan fixes the kernel: CUDA cores (one launch, every item a single
@@ -946,17 +974,15 @@ cudaError_t launch_merge(const RunArgs& a) {
   const int rows = a.hp->n_merge * a.hp->G;
   const int blocks = (rows + 7) / 8;
   const bool bf = a.hp->dtype == PA_BF16;
-  if (a.hp->D == 128) {
-    if (bf) merge_kernel<__nv_bfloat16, 128><<<blocks, 256, 0, a.stream>>>(kp, rows);
-    else merge_kernel<__half, 128><<<blocks, 256, 0, a.stream>>>(kp, rows);
-  } else if (a.hp->D == 256) {
-    if (bf) merge_kernel<__nv_bfloat16, 256><<<blocks, 256, 0, a.stream>>>(kp, rows);
-    else merge_kernel<__half, 256><<<blocks, 256, 0, a.stream>>>(kp, rows);
-  } else {
-    if (bf) merge_kernel<__nv_bfloat16, 64><<<blocks, 256, 0, a.stream>>>(kp, rows);
-    else merge_kernel<__half, 64><<<blocks, 256, 0, a.stream>>>(kp, rows);
-  }
-  return cudaGetLastError();
+  const unsigned nb = unsigned(blocks);
+  if (a.hp->D == 128)
+    return bf ? launch_pdl(merge_kernel<__nv_bfloat16, 128>, nb, 256u, size_t(0), a.stream, kp, rows)
+              : launch_pdl(merge_kernel<__half, 128>, nb, 256u, size_t(0), a.stream, kp, rows);
+  if (a.hp->D == 256)
+    return bf ? launch_pdl(merge_kernel<__nv_bfloat16, 256>, nb, 256u, size_t(0), a.stream, kp, rows)
+              : launch_pdl(merge_kernel<__half, 256>, nb, 256u, size_t(0), a.stream, kp, rows);
+  return bf ? launch_pdl(merge_kernel<__nv_bfloat16, 64>, nb, 256u, size_t(0), a.stream, kp, rows)
+            : launch_pdl(merge_kernel<__half, 64>, nb, 256u, size_t(0), a.stream, kp, rows);
 }
 
 cudaError_t launch_debug_gather(const RunArgs& a, int32_t* page_out, int32_t* slot_out) {

@@ -4,8 +4,10 @@
 #include <atomic>
 #include <cstddef>
 #include <cstdint>
+#include <cstring>
 #include <mutex>
 #include <string>
+#include <utility>
 #include <vector>
 
 #include <cuda.h>
@@ -79,6 +81,30 @@ inline cudaError_t set_smem_once(std::atomic<uint64_t>& done, const void* func, 
   e = cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
   if (e == cudaSuccess && bit) done.fetch_or(bit, std::memory_order_acq_rel);
   return e;
+}
+
+// Launch `kernel` on `stream` with programmatic stream serialization: it may
+// begin (and run its prologue) while the previous kernel on the stream
+// finishes; the kernel itself waits (pdl_wait) before touching data that
+// kernel may produce or read.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                              cudaStream_t stream, Args&&... args) {
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(block);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  std::memset(attr, 0, sizeof(attr));
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+#ifndef PA_NO_PDL
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+#endif
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
 // Error reporting into the thread-local last-error text (api.cu).

@@ -224,14 +224,6 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     if (warp == C::WARP_PROD && lane == 0) {
       tma_prefetch_desc(&q_map);
       if (use_tma) tma_prefetch_desc(&kv_map);
-      mbar_arrive_expect_tx(q_full, uint32_t((has_b ? 2 : 1) * C::Q_BYTES));
-#pragma unroll
-      for (int kb = 0; kb < NKB; ++kb) {
-        tma_load_3d(q_addr(0) + kb * C::BLK, &q_map, kb * 64, it.kv_head * G, rq.qo_start + it.q_tok0, q_full);
-        if (has_b)
-          tma_load_3d(q_addr(1) + kb * C::BLK, &q_map, kb * 64, it.kv_head * G, rq.qo_start + it.q_tok0 + TQ,
-                      q_full);
-      }
     }
     const int ps = p.ps, sh = p.ps_shift;
     // TMA path: lane l gathers page l of every key tile (at most 16 pages of
@@ -246,6 +238,17 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       return lane < npgj ? __ldg(p.pages + rq.page_start + (k0j >> sh) + lane) : 0;
     };
     int pid_j = tile_pid(0), pid_j1 = tile_pid(1);
+    pdl_wait();  // q and the cache may come from the previous kernel on the stream
+    if (warp == C::WARP_PROD && lane == 0) {
+      mbar_arrive_expect_tx(q_full, uint32_t((has_b ? 2 : 1) * C::Q_BYTES));
+#pragma unroll
+      for (int kb = 0; kb < NKB; ++kb) {
+        tma_load_3d(q_addr(0) + kb * C::BLK, &q_map, kb * 64, it.kv_head * G, rq.qo_start + it.q_tok0, q_full);
+        if (has_b)
+          tma_load_3d(q_addr(1) + kb * C::BLK, &q_map, kb * 64, it.kv_head * G, rq.qo_start + it.q_tok0 + TQ,
+                      q_full);
+      }
+    }
     int issued_k = 0, issued_v = 0;
     bool ok = true;
     for (int j = 0; ok && j < nkt; ++j) {
@@ -571,7 +574,9 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     for (int j = 1; ok && j < nkt; ++j) ok = tile(j, std::false_type{});
 
     // ---------------------------------------------------------------- epilogue
+    pdl_wait();  // (long since returned for the producer) before the first global write
     if (ok && (x == 0 || has_b)) ok = warp_wait(&o_done[x], 0, abort_flag, p.status, p.wait_limit);
+    pdl_launch();
     if (ok && (x == 0 || has_b)) {
       tc_fence_after();
       const float m_use = (m_ref == -INFINITY) ? 0.f : m_ref;
@@ -634,8 +639,8 @@ cudaError_t launch_prefill_t(const RunArgs& a, const CUtensorMap* kv_map, const 
   static std::atomic<uint64_t> attr_set{0};
   cudaError_t e = set_smem_once(attr_set, reinterpret_cast<const void*>(prefill_kernel<T, D, NT>), C::SMEM);
   if (e != cudaSuccess) return e;
-  prefill_kernel<T, D, NT><<<a.hp->n_pre, C::THREADS, C::SMEM, a.stream>>>(*kv_map, *q_map, kp, use_tma);
-  return cudaGetLastError();
+  return launch_pdl(prefill_kernel<T, D, NT>, unsigned(a.hp->n_pre), unsigned(C::THREADS), size_t(C::SMEM), a.stream,
+                    *kv_map, *q_map, kp, use_tma);
 }
 
 template <typename T>
