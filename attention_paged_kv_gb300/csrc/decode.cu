@@ -80,15 +80,16 @@ __device__ __forceinline__ uint32_t sw_off(int t, int c) {
 // Producer warp of the decode kernels: streams the item's keys in 64-key
 // stages (K then V, 128-byte-swizzled rows) into NST buffers, by TMA
 // through the page table or, for pages of fewer than 8 slots, by cp.async.
-// With TMA it copies the halves [h0, h1) of each stage (0 = K, 1 = V), so two
-// producer warps can share a stage's copies; each then arrives on the
-// stage's full barrier with its own byte count.  On return every copy it
+// With TMA it copies the halves [h0, h1) of each stage (0 = K, 1 = V) and
+// the 64-column blocks [kb0, kb1) of each row, so several producer warps can
+// share a stage's copies; each then arrives on the stage's full barrier with
+// its own byte count.  On return every copy it
 // issued has landed (or its wait gave up).
 template <typename T, int D, int NST = kDecStages>
 __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const KParams& p, const DecItem& it,
                                                const ReqEntry& rq, uint8_t* smem, uint64_t* full, uint64_t* empty,
                                                volatile int32_t* abort_flag, int use_tma, int nstage, int lane,
-                                               int h0 = 0, int h1 = 2) {
+                                               int h0 = 0, int h1 = 2, int kb0 = 0, int kb1 = DecCfg<D>::NKB) {
   using C = DecCfg<D, NST>;
   constexpr int NKB = C::NKB;
   constexpr int NCH = D / 8;
@@ -129,7 +130,7 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
       const uint32_t kdst = sbase + st * C::STAGE;
       if (use_tma) {
         const int nbox = (s1 - s0 + BR - 1) >> br_shift;
-        if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(nbox * BR * 128 * NKB * (h1 - h0)));
+        if (lane == 0) mbar_arrive_expect_tx(&full[st], uint32_t(nbox * BR * 128 * (kb1 - kb0) * (h1 - h0)));
         __syncwarp();
         if (lane < nbox) {
           const int slot = (s0 + lane * BR) & (p.ps - 1);
@@ -139,6 +140,7 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
           }
 #pragma unroll
           for (int kb = 0; kb < NKB; ++kb) {
+            if (kb < kb0 || kb >= kb1) continue;
             if (h0 == 0)
               tma_kv_rows(kdst + kb * C::BLK + lane * BR * 128, &kv_map, kb * 64, it.kv_head, slot, 2 * pid,
                           &full[st], p.hnd);
@@ -449,11 +451,14 @@ __global__ void __launch_bounds__(kDecThreads, (NST <= 3 ? 2 : 1))
 // r = token * G + head of an item are the M rows of m16n8k16 fragments, so
 // S = q K^T needs no reshaping:
 //   warps 4-5  the producer of the CUDA-core kernel (64-key stages, 128-byte
-//              swizzled rows), split in two: warp 4 copies the stages' K,
-//              warp 5 their V (each TMA copy costs its issuing thread ~90
-//              cycles when the data comes from HBM, and one warp issuing
-//              all copies limited a CTA's stream: mixed-batch decode 0.712
-//              -> 0.698 ms).  With cp.async staging warp 4 copies both.
+//   (or 4-7)   swizzled rows), split in two: warp 4 copies the stages' K,
+//              warp 5 their V (each TMA copy costs its issuing warp ~110
+//              cycles, and one warp issuing all copies limited a CTA's
+//              stream: mixed-batch decode 0.712 -> 0.698 ms).  Launches of
+//              one CTA per SM at head_dim 128 split each half again by
+//              64-column block over four warps (two warps' issue time still
+//              set the pace there: decode timing script 14.6 -> 13.9 us).
+//              With cp.async staging warp 4 copies everything.
 //   warps 0-3  row group rg = warp % RGN (16 rows each), key subset
 //              kq = warp / RGN of every stage: with RGN row groups each warp
 //              takes 16 * RGN of the stage's 64 keys.  ldmatrix feeds K from
@@ -499,8 +504,14 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "memory");
 }
 
-constexpr int kDmProds = 2;                        // producer warps: one copies K, one V
-constexpr int kDmThreads = 32 * (4 + kDmProds);    // 4 MMA warps + producer(s)
+// Producer warps of the small-query kernel: two (K, V) when two CTAs share
+// an SM; four (K and V of each 64-column block) in the one-CTA-per-SM
+// launches at head_dim 128, where each producer warp's issue time (about
+// 110 cycles a copy, 8 copies of a stage for one warp) set the pace.
+template <int D, int NST>
+__host__ __device__ constexpr int dm_prods() { return (NST > kDecStages && D >= 128) ? 4 : 2; }
+template <int D, int NST>
+__host__ __device__ constexpr int dm_threads() { return 32 * (4 + dm_prods<D, NST>()); }
 
 template <int RC>
 struct RowClass {
@@ -512,11 +523,12 @@ struct RowClass {
 };
 
 template <typename T, int D, int RC, int NST>
-__global__ void __launch_bounds__(kDmThreads, NST <= 3 ? 2 : 1)
+__global__ void __launch_bounds__(dm_threads<D, NST>(), NST <= 3 ? 2 : 1)
     decode_mma_kernel(const __grid_constant__ CUtensorMap kv_map, const KParams p, const int use_tma,
                       const int item0) {
   using C = DecCfg<D, NST>;
   using RCl = RowClass<RC>;
+  constexpr int PRODS = dm_prods<D, NST>(), THREADS = dm_threads<D, NST>();
   constexpr int RGN = RCl::RGN, KS = RCl::KS, KW = RCl::KW, NKB = RCl::NKB;
   constexpr int NA = 4;        // fragment registers per lane: rows lo (0, 1) and hi (2, 3)
   constexpr int NKS = D / 16;  // k-steps of S
@@ -536,7 +548,7 @@ __global__ void __launch_bounds__(kDmThreads, NST <= 3 ? 2 : 1)
 
   if (tid == 0) {
     for (int i = 0; i < NST; ++i) {
-      mbar_init(&full[i], use_tma ? kDmProds : 32);
+      mbar_init(&full[i], use_tma ? PRODS : 32);
       mbar_init(&empty[i], 4);
     }
     mbar_init(never, 1);
@@ -546,14 +558,18 @@ __global__ void __launch_bounds__(kDmThreads, NST <= 3 ? 2 : 1)
   __syncthreads();
 
   if (warp >= 4) {
-    // with two producer warps and TMA staging, warp 4 copies K and warp 5 V;
-    // cp.async staging (pages of < 8 slots) stays with warp 4 alone
+    // with TMA staging producer warp 4 + w copies half w % 2 (K, V) of every
+    // stage, and with four producers column block w / 2 of it; cp.async
+    // staging (pages of < 8 slots) stays with warp 4 alone
     if (warp == 4 || use_tma) {
-      const int h0 = (kDmProds == 2 && use_tma && warp == 5) ? 1 : 0;
-      const int h1 = (kDmProds == 2 && use_tma && warp == 4) ? 1 : 2;
-      decode_produce<T, D, NST>(kv_map, p, it, rq, smem, full, empty, abort_flag, use_tma, nstage, lane, h0, h1);
+      const int w = warp - 4;
+      const int h0 = use_tma ? (w & 1) : 0, h1 = use_tma ? (w & 1) + 1 : 2;
+      const int kb0 = (use_tma && PRODS == 4) ? (w >> 1) : 0;
+      const int kb1 = (use_tma && PRODS == 4) ? (w >> 1) + 1 : C::NKB;
+      decode_produce<T, D, NST>(kv_map, p, it, rq, smem, full, empty, abort_flag, use_tma, nstage, lane, h0, h1,
+                                kb0, kb1);
     }
-    asm volatile("bar.arrive 1, %0;" ::"n"(kDmThreads) : "memory");
+    asm volatile("bar.arrive 1, %0;" ::"n"(THREADS) : "memory");
     return;
   }
 
@@ -739,7 +755,7 @@ __global__ void __launch_bounds__(kDmThreads, NST <= 3 ? 2 : 1)
   l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  asm volatile("bar.sync 1, %0;" ::"n"(kDmThreads) : "memory");  // stage memory is free from here
+  asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");  // stage memory is free from here
   float* comb_o = reinterpret_cast<float*>(smem);  // [4 warps][16 rows][D]
   float* comb_m = comb_o + 4 * 16 * D;             // [4][16]
   float* comb_l = comb_m + 4 * 16;                 // [4][16]
@@ -898,7 +914,7 @@ cudaError_t launch_mma_n(const RunArgs& a, const CUtensorMap* map, const KParams
   static std::atomic<uint64_t> attr_set{0};
   cudaError_t e = set_smem_once(attr_set, reinterpret_cast<const void*>(decode_mma_kernel<T, D, RC, NST>), C::SMEM);
   if (e != cudaSuccess) return e;
-  return launch_pdl(decode_mma_kernel<T, D, RC, NST>, unsigned(n), unsigned(kDmThreads), size_t(C::SMEM), a.stream,
+  return launch_pdl(decode_mma_kernel<T, D, RC, NST>, unsigned(n), unsigned(dm_threads<D, NST>()), size_t(C::SMEM), a.stream,
                     *map, kp, use_tma, item0);
 }
 
