@@ -583,31 +583,48 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
       const float inv_l = l_sum > 0.f ? 1.f / l_sum : 0.f;
       const float lse_v = l_sum > 0.f ? (m_use + __log2f(l_sum)) * kLn2 : -INFINITY;
       const bool partial = it.part_row >= 0;
+      // O_x columns [32 c, 32 c + 32) of the row, scaled and written out
+      auto store_chunk = [&](int c4, const uint32_t (&o)[32]) {
+        if (!row_valid) return;
+        if (!partial) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + qrow * D + c4 * 32);
 #pragma unroll
-      for (int c4 = 0; c4 < D / 32; ++c4) {
-        uint32_t o[32];
-        tmem_ld32(o_col + c4 * 32, o);
-        tmem_wait_ld(o);
-        if (row_valid) {
-          if (!partial) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<T*>(p.out) + qrow * D + c4 * 32);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-              uint4 w;
-              w.x = Elt<T>::from_f2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
-              w.y = Elt<T>::from_f2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
-              w.z = Elt<T>::from_f2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
-              w.w = Elt<T>::from_f2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
-              dst[v] = w;
-            }
-          } else {
-            float4* dst =
-                reinterpret_cast<float4*>(p.part_o + (int64_t(it.part_row) + x * kQRows + r) * D + c4 * 32);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              dst[v] = make_float4(__uint_as_float(o[4 * v + 0]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
-                                   __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+          for (int v = 0; v < 4; ++v) {
+            uint4 w;
+            w.x = Elt<T>::from_f2(__uint_as_float(o[8 * v + 0]) * inv_l, __uint_as_float(o[8 * v + 1]) * inv_l);
+            w.y = Elt<T>::from_f2(__uint_as_float(o[8 * v + 2]) * inv_l, __uint_as_float(o[8 * v + 3]) * inv_l);
+            w.z = Elt<T>::from_f2(__uint_as_float(o[8 * v + 4]) * inv_l, __uint_as_float(o[8 * v + 5]) * inv_l);
+            w.w = Elt<T>::from_f2(__uint_as_float(o[8 * v + 6]) * inv_l, __uint_as_float(o[8 * v + 7]) * inv_l);
+            dst[v] = w;
           }
+        } else {
+          float4* dst =
+              reinterpret_cast<float4*>(p.part_o + (int64_t(it.part_row) + x * kQRows + r) * D + c4 * 32);
+#pragma unroll
+          for (int v = 0; v < 8; ++v)
+            dst[v] = make_float4(__uint_as_float(o[4 * v + 0]) * inv_l, __uint_as_float(o[4 * v + 1]) * inv_l,
+                                 __uint_as_float(o[4 * v + 2]) * inv_l, __uint_as_float(o[4 * v + 3]) * inv_l);
+        }
+      };
+      if constexpr (D <= 128) {
+        // the whole O row in registers with one wait, then the stores
+        uint32_t o[D / 32][32];
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) tmem_ld32(o_col + c4 * 32, o[c4]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4)
+#pragma unroll
+          for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(o[c4][i]));
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) store_chunk(c4, o[c4]);
+      } else {
+#pragma unroll
+        for (int c4 = 0; c4 < D / 32; ++c4) {
+          uint32_t o[32];
+          tmem_ld32(o_col + c4 * 32, o);
+          tmem_wait_ld(o);
+          store_chunk(c4, o);
         }
       }
       if (row_valid) {
