@@ -503,6 +503,13 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "r"(addr)
                : "memory");
 }
+// 8x8 transpose of 16-bit elements across the warp: lane (g, t) holds
+// elements (g, 2t) and (g, 2t + 1) before and after
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
 
 // Producer warps of the small-query kernel: two (K, V) when two CTAs share
 // an SM; four (K and V of each 64-column block) in the one-CTA-per-SM
@@ -591,184 +598,323 @@ __global__ void __launch_bounds__(dm_threads<D, NST>(), NST <= 3 ? 2 : 1)
     return min(it.tok1, lim);
   };
   const int end_lo = end_of(r_lo), end_hi = end_of(r_hi);
+  float* comb_o = reinterpret_cast<float*>(smem);  // [4 warps][16 rows][D], over the stages at the end
+  float* comb_m = comb_o + 4 * 16 * D;             // [4][16]
+  float* comb_l = comb_m + 4 * 16;                 // [4][16]
 
-  // q as A fragments: {row lo cols 2t, row lo cols 2t+8, row hi cols 2t, row hi cols 2t+8} per k-step
-  uint32_t qa[NKS][NA];
-  {
-    const T* q = static_cast<const T*>(p.q);
+  if constexpr (RC == 0) {
+    // Up to 8 packed rows: S^T = K q^T and O^T = V^T P^T, so the 16-row (M)
+    // side of each m16n8k16 holds keys or head-dim columns and its 8-column
+    // (N) side the packed rows: no MMA row idles (the direct form below
+    // fills 8 of its 16 rows, twice the MMAs a stage).  Warp w takes keys
+    // 16w .. 16w + 15 of every stage; lane (g, t) holds S^T of keys g and
+    // g + 8 for rows 2t and 2t + 1, and O^T of columns g and g + 8 of each
+    // 16-column block for the same two rows.  P^T reaches the B operand of
+    // O^T through 8x8 transposes in registers.
+    constexpr int NMT = D / 16;  // 16-column blocks of O^T
+    const int kofs = warp * 16;
+    const int ra = 2 * t, rb = 2 * t + 1;
+    const int end_a = end_of(ra), end_b = end_of(rb);
+    // q^T as B fragments: {q[row g][16 kk + 2t ..], q[row g][16 kk + 2t + 8 ..]}
+    uint32_t qb[NKS][2];
 #pragma unroll
-    for (int kk = 0; kk < NKS; ++kk) qa[kk][0] = qa[kk][1] = 0u;
-    if (r_lo < R) {
-      const uint32_t* qp = reinterpret_cast<const uint32_t*>(q + row_of(r_lo) * D);
+    for (int kk = 0; kk < NKS; ++kk) qb[kk][0] = qb[kk][1] = 0u;
+    if (g < R) {
+      const uint32_t* qp = reinterpret_cast<const uint32_t*>(static_cast<const T*>(p.q) + row_of(g) * D);
 #pragma unroll
       for (int kk = 0; kk < NKS; ++kk) {
-        qa[kk][0] = __ldg(qp + kk * 8 + t);
-        qa[kk][1] = __ldg(qp + kk * 8 + 4 + t);
+        qb[kk][0] = __ldg(qp + kk * 8 + t);
+        qb[kk][1] = __ldg(qp + kk * 8 + 4 + t);
       }
     }
+    float ot[NMT][4];  // {col 16m + g: rows a, b; col 16m + g + 8: rows a, b}
 #pragma unroll
-    for (int kk = 0; kk < NKS; ++kk) qa[kk][2] = qa[kk][3] = 0u;
-    if (r_hi < R) {
-      const uint32_t* qp = reinterpret_cast<const uint32_t*>(q + row_of(r_hi) * D);
+    for (int m = 0; m < NMT; ++m)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) ot[m][e] = 0.f;
+    float m_a = -INFINITY, m_b = -INFINITY;
+    float l_a = 0.f, l_b = 0.f;  // sums over this lane's keys only
+    const bool split_p = rq.kv_len < 128;
+    const float sl2 = p.scale_log2;
+    for (int j = 0; j < nstage; ++j) {
+      const int st = j % NST;
+      const bool ok = mbar_wait(&full[st], (j / NST) & 1, abort_flag, p.status, p.wait_limit);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int s0 = it.tok0 + j * kDecTile;
+      const int nval = min(kDecTile, it.tok1 - s0);
+      const uint32_t kbase = smem_u32(smem) + st * C::STAGE;
+      const uint32_t vbase = kbase + C::STAGE_K;
+      float sc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int kk = 0; kk < NKS; ++kk) {
-        qa[kk][2] = __ldg(qp + kk * 8 + t);
-        qa[kk][3] = __ldg(qp + kk * 8 + 4 + t);
+        uint32_t a[4];
+        ldsm_x4(kbase + sw_off<D>(kofs + (mi >> 1) * 8 + ri, 2 * kk + (mi & 1)), a[0], a[1], a[2], a[3]);
+        Mma<T>::run(sc, a, qb[kk][0], qb[kk][1]);
       }
-    }
-  }
-  float o[NNT][NA];  // rows lo (regs 0, 1) and hi (2, 3); columns 8n + 2t, 8n + 2t + 1
+      // each row's keys end at its own causal limit
+      const int key0 = s0 + kofs + g, key1 = key0 + 8;
+      sc[0] = key0 < end_a ? sc[0] * sl2 : -INFINITY;
+      sc[1] = key0 < end_b ? sc[1] * sl2 : -INFINITY;
+      sc[2] = key1 < end_a ? sc[2] * sl2 : -INFINITY;
+      sc[3] = key1 < end_b ? sc[3] * sl2 : -INFINITY;
+      float mx_a = fmaxf(sc[0], sc[2]), mx_b = fmaxf(sc[1], sc[3]);
 #pragma unroll
-  for (int n = 0; n < NNT; ++n)
-#pragma unroll
-    for (int e = 0; e < NA; ++e) o[n][e] = 0.f;
-  float m_lo = -INFINITY, m_hi = -INFINITY;
-  float l_lo = 0.f, l_hi = 0.f;  // sums over this lane's columns only
-  const bool split_p = rq.kv_len < 128;
-  const float sl2 = p.scale_log2;
-  const int kofs = kq * KW;  // this warp's first key in every stage
-
-  for (int j = 0; j < nstage; ++j) {
-    const int st = j % NST;
-    const bool ok = mbar_wait(&full[st], (j / NST) & 1, abort_flag, p.status, p.wait_limit);
-    if (!__all_sync(0xffffffffu, ok)) break;
-    const int s0 = it.tok0 + j * kDecTile;         // absolute position of the stage's first key
-    const int nval = min(kDecTile, it.tok1 - s0);  // keys of the stage inside the item's range
-    const uint32_t kbase = smem_u32(smem) + st * C::STAGE;
-    const uint32_t vbase = kbase + C::STAGE_K;
-
-    // S = q K^T for keys kofs .. kofs + KW - 1 of the stage (n-tiles of 8 keys)
-    float sc[2 * NKB][NA];
-#pragma unroll
-    for (int n = 0; n < 2 * NKB; ++n)
-#pragma unroll
-      for (int e = 0; e < NA; ++e) sc[n][e] = 0.f;
-#pragma unroll
-    for (int kk = 0; kk < NKS; ++kk) {
-#pragma unroll
-      for (int kb = 0; kb < NKB; ++kb) {
-        uint32_t b00, b01, b10, b11;
-        ldsm_x4(kbase + sw_off<D>(kofs + kb * 16 + (mi >> 1) * 8 + ri, 2 * kk + (mi & 1)), b00, b01, b10, b11);
-        Mma<T>::run(sc[2 * kb], qa[kk], b00, b01);
-        Mma<T>::run(sc[2 * kb + 1], qa[kk], b10, b11);
+      for (int sh = 4; sh < 32; sh <<= 1) {
+        mx_a = fmaxf(mx_a, __shfl_xor_sync(0xffffffffu, mx_a, sh));
+        mx_b = fmaxf(mx_b, __shfl_xor_sync(0xffffffffu, mx_b, sh));
       }
-    }
-
-    // online softmax on the fragment: this lane holds keys 8n + 2t + e of rows lo and hi
-    float mx_lo = -INFINITY, mx_hi = -INFINITY;
+      // a row that has seen no key yet keeps O = 0 and needs no rescale
+      const float mn_a = fmaxf(m_a, mx_a), mn_b = fmaxf(m_b, mx_b);
+      const float mu_a = (mn_a == -INFINITY) ? 0.f : mn_a;
+      const float mu_b = (mn_b == -INFINITY) ? 0.f : mn_b;
+      const float al_a = (mn_a == -INFINITY) ? 1.f : ex2f(m_a - mu_a);
+      const float al_b = (mn_b == -INFINITY) ? 1.f : ex2f(m_b - mu_b);
+      m_a = mn_a;
+      m_b = mn_b;
+      const float p0 = ex2f(sc[0] - mu_a), p1 = ex2f(sc[1] - mu_b);
+      const float p2 = ex2f(sc[2] - mu_a), p3 = ex2f(sc[3] - mu_b);
+      l_a = l_a * al_a + (p0 + p2);
+      l_b = l_b * al_b + (p1 + p3);
+      if (__any_sync(0xffffffffu, al_a != 1.f || al_b != 1.f)) {
 #pragma unroll
-    for (int n = 0; n < 2 * NKB; ++n)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int key = s0 + kofs + n * 8 + 2 * t + e;
-        sc[n][e] = key < end_lo ? sc[n][e] * sl2 : -INFINITY;
-        mx_lo = fmaxf(mx_lo, sc[n][e]);
-        sc[n][2 + e] = key < end_hi ? sc[n][2 + e] * sl2 : -INFINITY;
-        mx_hi = fmaxf(mx_hi, sc[n][2 + e]);
-      }
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
-    mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
-    mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
-    // a row that has seen no key yet keeps O = 0 and needs no rescale (alpha 1)
-    const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
-    const float mu_lo = (mn_lo == -INFINITY) ? 0.f : mn_lo;
-    const float mu_hi = (mn_hi == -INFINITY) ? 0.f : mn_hi;
-    const float al_lo = (mn_lo == -INFINITY) ? 1.f : ex2f(m_lo - mu_lo);
-    const float al_hi = (mn_hi == -INFINITY) ? 1.f : ex2f(m_hi - mu_hi);
-    m_lo = mn_lo;
-    m_hi = mn_hi;
-    float ps_lo = 0.f, ps_hi = 0.f;
-#pragma unroll
-    for (int n = 0; n < 2 * NKB; ++n)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        sc[n][e] = ex2f(sc[n][e] - mu_lo);
-        ps_lo += sc[n][e];
-        sc[n][2 + e] = ex2f(sc[n][2 + e] - mu_hi);
-        ps_hi += sc[n][2 + e];
-      }
-    l_lo = l_lo * al_lo + ps_lo;
-    l_hi = l_hi * al_hi + ps_hi;
-    if (__any_sync(0xffffffffu, al_lo != 1.f || al_hi != 1.f)) {
-#pragma unroll
-      for (int n = 0; n < NNT; ++n) {
-        o[n][0] *= al_lo;
-        o[n][1] *= al_lo;
-        o[n][2] *= al_hi;
-        o[n][3] *= al_hi;
-      }
-    }
-
-    // P as A fragments of P V, one per 16-key block (n-tiles 2kb, 2kb + 1),
-    // plus the rounding remainder when P is split
-    uint32_t pa[NKB][NA], la[NKB][NA];
-#pragma unroll
-    for (int kb = 0; kb < NKB; ++kb)
-#pragma unroll
-      for (int x = 0; x < NA; ++x) {
-        // x = 0, 1: row lo, keys 2t.. and 8 + 2t..; x = 2, 3: row hi
-        const float v0 = sc[2 * kb + (x & 1)][(x >> 1) * 2];
-        const float v1 = sc[2 * kb + (x & 1)][(x >> 1) * 2 + 1];
-        pa[kb][x] = Elt<T>::from_f2(v0, v1);
-        la[kb][x] = 0u;
-        if (split_p) {
-          const float2 h = Elt<T>::to_f2(pa[kb][x]);
-          la[kb][x] = Elt<T>::from_f2(v0 - h.x, v1 - h.y);
+        for (int m = 0; m < NMT; ++m) {
+          ot[m][0] *= al_a;
+          ot[m][1] *= al_b;
+          ot[m][2] *= al_a;
+          ot[m][3] *= al_b;
         }
       }
-
-    // O += P V; V rows of keys past the range (other data, or stale stage
-    // contents: possibly NaN) are zeroed in the fragments, since 0 * NaN = NaN
-    const bool vpart = nval < kofs + KW;
-#pragma unroll
-    for (int kb = 0; kb < NKB; ++kb) {
+      // P^T as B fragments ({keys 2t, 2t + 1 | row g}, {keys 2t + 8, 2t + 9 |
+      // row g}), plus the rounding remainder when P is split
+      const uint32_t x0 = Elt<T>::from_f2(p0, p1), x1 = Elt<T>::from_f2(p2, p3);
+      const uint32_t pb0 = movm_t(x0), pb1 = movm_t(x1);
+      uint32_t lb0 = 0u, lb1 = 0u;
+      if (split_p) {
+        const float2 h0 = Elt<T>::to_f2(x0), h1 = Elt<T>::to_f2(x1);
+        lb0 = movm_t(Elt<T>::from_f2(p0 - h0.x, p1 - h0.y));
+        lb1 = movm_t(Elt<T>::from_f2(p2 - h1.x, p3 - h1.y));
+      }
+      // O^T += V^T P^T; V rows past the range (other data, or stale stage
+      // contents: possibly NaN) are zeroed in the fragments
       uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-      if (vpart) {
-        const int k0 = kofs + kb * 16 + 2 * t;  // ldmatrix.trans: this lane's keys 2t, 2t+1 (+8)
+      if (nval < kofs + 16) {
+        const int k0 = kofs + 2 * t;  // ldmatrix.trans: this lane's keys 2t, 2t + 1 (+ 8)
         mlo = (k0 < nval ? 0x0000ffffu : 0u) | (k0 + 1 < nval ? 0xffff0000u : 0u);
         mhi = (k0 + 8 < nval ? 0x0000ffffu : 0u) | (k0 + 9 < nval ? 0xffff0000u : 0u);
       }
 #pragma unroll
-      for (int dp = 0; dp < NNT / 2; ++dp) {
-        uint32_t v0, v1, v2, v3;
-        ldsm_x4_t(vbase + sw_off<D>(kofs + kb * 16 + (mi & 1) * 8 + ri, 2 * dp + (mi >> 1)), v0, v1, v2, v3);
-        v0 &= mlo;
-        v1 &= mhi;
-        v2 &= mlo;
-        v3 &= mhi;
-        Mma<T>::run(o[2 * dp], pa[kb], v0, v1);
-        Mma<T>::run(o[2 * dp + 1], pa[kb], v2, v3);
-        if (split_p) {
-          Mma<T>::run(o[2 * dp], la[kb], v0, v1);
-          Mma<T>::run(o[2 * dp + 1], la[kb], v2, v3);
+      for (int m = 0; m < NMT; ++m) {
+        uint32_t a[4];
+        ldsm_x4_t(vbase + sw_off<D>(kofs + (mi & 1) * 8 + ri, 2 * m + (mi >> 1)), a[0], a[1], a[2], a[3]);
+        a[0] &= mlo;
+        a[1] &= mhi;
+        a[2] &= mlo;
+        a[3] &= mhi;
+        Mma<T>::run(ot[m], a, pb0, pb1);
+        if (split_p) Mma<T>::run(ot[m], a, lb0, lb1);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    pdl_launch();
+    // ---------------------------------------------------------------- combine the key subsets
+#pragma unroll
+    for (int sh = 4; sh < 32; sh <<= 1) {
+      l_a += __shfl_xor_sync(0xffffffffu, l_a, sh);
+      l_b += __shfl_xor_sync(0xffffffffu, l_b, sh);
+    }
+    asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");  // stage memory is free from here
+#pragma unroll
+    for (int m = 0; m < NMT; ++m) {
+      comb_o[(warp * 16 + ra) * D + 16 * m + g] = ot[m][0];
+      comb_o[(warp * 16 + rb) * D + 16 * m + g] = ot[m][1];
+      comb_o[(warp * 16 + ra) * D + 16 * m + g + 8] = ot[m][2];
+      comb_o[(warp * 16 + rb) * D + 16 * m + g + 8] = ot[m][3];
+    }
+    if (g == 0) {
+      comb_m[warp * 16 + ra] = m_a;
+      comb_l[warp * 16 + ra] = l_a;
+      comb_m[warp * 16 + rb] = m_b;
+      comb_l[warp * 16 + rb] = l_b;
+    }
+  } else {
+
+    // q as A fragments: {row lo cols 2t, row lo cols 2t+8, row hi cols 2t, row hi cols 2t+8} per k-step
+    uint32_t qa[NKS][NA];
+    {
+      const T* q = static_cast<const T*>(p.q);
+#pragma unroll
+      for (int kk = 0; kk < NKS; ++kk) qa[kk][0] = qa[kk][1] = 0u;
+      if (r_lo < R) {
+        const uint32_t* qp = reinterpret_cast<const uint32_t*>(q + row_of(r_lo) * D);
+#pragma unroll
+        for (int kk = 0; kk < NKS; ++kk) {
+          qa[kk][0] = __ldg(qp + kk * 8 + t);
+          qa[kk][1] = __ldg(qp + kk * 8 + 4 + t);
+        }
+      }
+#pragma unroll
+      for (int kk = 0; kk < NKS; ++kk) qa[kk][2] = qa[kk][3] = 0u;
+      if (r_hi < R) {
+        const uint32_t* qp = reinterpret_cast<const uint32_t*>(q + row_of(r_hi) * D);
+#pragma unroll
+        for (int kk = 0; kk < NKS; ++kk) {
+          qa[kk][2] = __ldg(qp + kk * 8 + t);
+          qa[kk][3] = __ldg(qp + kk * 8 + 4 + t);
         }
       }
     }
-    __syncwarp();
-    if (lane == 0) mbar_arrive(&empty[st]);
-  }
-
-  pdl_launch();
-  // ---------------------------------------------------------------- combine the key subsets
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
-  l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
-  l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
-  asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");  // stage memory is free from here
-  float* comb_o = reinterpret_cast<float*>(smem);  // [4 warps][16 rows][D]
-  float* comb_m = comb_o + 4 * 16 * D;             // [4][16]
-  float* comb_l = comb_m + 4 * 16;                 // [4][16]
+    float o[NNT][NA];  // rows lo (regs 0, 1) and hi (2, 3); columns 8n + 2t, 8n + 2t + 1
 #pragma unroll
-  for (int n = 0; n < NNT; ++n) {
-    *reinterpret_cast<float2*>(&comb_o[(warp * 16 + g) * D + n * 8 + 2 * t]) = make_float2(o[n][0], o[n][1]);
-    *reinterpret_cast<float2*>(&comb_o[(warp * 16 + g + 8) * D + n * 8 + 2 * t]) = make_float2(o[n][2], o[n][3]);
-  }
-  if (t == 0) {
-    comb_m[warp * 16 + g] = m_lo;
-    comb_l[warp * 16 + g] = l_lo;
-    comb_m[warp * 16 + g + 8] = m_hi;
-    comb_l[warp * 16 + g + 8] = l_hi;
+    for (int n = 0; n < NNT; ++n)
+#pragma unroll
+      for (int e = 0; e < NA; ++e) o[n][e] = 0.f;
+    float m_lo = -INFINITY, m_hi = -INFINITY;
+    float l_lo = 0.f, l_hi = 0.f;  // sums over this lane's columns only
+    const bool split_p = rq.kv_len < 128;
+    const float sl2 = p.scale_log2;
+    const int kofs = kq * KW;  // this warp's first key in every stage
+
+    for (int j = 0; j < nstage; ++j) {
+      const int st = j % NST;
+      const bool ok = mbar_wait(&full[st], (j / NST) & 1, abort_flag, p.status, p.wait_limit);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      const int s0 = it.tok0 + j * kDecTile;         // absolute position of the stage's first key
+      const int nval = min(kDecTile, it.tok1 - s0);  // keys of the stage inside the item's range
+      const uint32_t kbase = smem_u32(smem) + st * C::STAGE;
+      const uint32_t vbase = kbase + C::STAGE_K;
+
+      // S = q K^T for keys kofs .. kofs + KW - 1 of the stage (n-tiles of 8 keys)
+      float sc[2 * NKB][NA];
+#pragma unroll
+      for (int n = 0; n < 2 * NKB; ++n)
+#pragma unroll
+        for (int e = 0; e < NA; ++e) sc[n][e] = 0.f;
+#pragma unroll
+      for (int kk = 0; kk < NKS; ++kk) {
+#pragma unroll
+        for (int kb = 0; kb < NKB; ++kb) {
+          uint32_t b00, b01, b10, b11;
+          ldsm_x4(kbase + sw_off<D>(kofs + kb * 16 + (mi >> 1) * 8 + ri, 2 * kk + (mi & 1)), b00, b01, b10, b11);
+          Mma<T>::run(sc[2 * kb], qa[kk], b00, b01);
+          Mma<T>::run(sc[2 * kb + 1], qa[kk], b10, b11);
+        }
+      }
+
+      // online softmax on the fragment: this lane holds keys 8n + 2t + e of rows lo and hi
+      float mx_lo = -INFINITY, mx_hi = -INFINITY;
+#pragma unroll
+      for (int n = 0; n < 2 * NKB; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int key = s0 + kofs + n * 8 + 2 * t + e;
+          sc[n][e] = key < end_lo ? sc[n][e] * sl2 : -INFINITY;
+          mx_lo = fmaxf(mx_lo, sc[n][e]);
+          sc[n][2 + e] = key < end_hi ? sc[n][2 + e] * sl2 : -INFINITY;
+          mx_hi = fmaxf(mx_hi, sc[n][2 + e]);
+        }
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 1));
+      mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, 2));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 1));
+      mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, 2));
+      // a row that has seen no key yet keeps O = 0 and needs no rescale (alpha 1)
+      const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+      const float mu_lo = (mn_lo == -INFINITY) ? 0.f : mn_lo;
+      const float mu_hi = (mn_hi == -INFINITY) ? 0.f : mn_hi;
+      const float al_lo = (mn_lo == -INFINITY) ? 1.f : ex2f(m_lo - mu_lo);
+      const float al_hi = (mn_hi == -INFINITY) ? 1.f : ex2f(m_hi - mu_hi);
+      m_lo = mn_lo;
+      m_hi = mn_hi;
+      float ps_lo = 0.f, ps_hi = 0.f;
+#pragma unroll
+      for (int n = 0; n < 2 * NKB; ++n)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          sc[n][e] = ex2f(sc[n][e] - mu_lo);
+          ps_lo += sc[n][e];
+          sc[n][2 + e] = ex2f(sc[n][2 + e] - mu_hi);
+          ps_hi += sc[n][2 + e];
+        }
+      l_lo = l_lo * al_lo + ps_lo;
+      l_hi = l_hi * al_hi + ps_hi;
+      if (__any_sync(0xffffffffu, al_lo != 1.f || al_hi != 1.f)) {
+#pragma unroll
+        for (int n = 0; n < NNT; ++n) {
+          o[n][0] *= al_lo;
+          o[n][1] *= al_lo;
+          o[n][2] *= al_hi;
+          o[n][3] *= al_hi;
+        }
+      }
+
+      // P as A fragments of P V, one per 16-key block (n-tiles 2kb, 2kb + 1),
+      // plus the rounding remainder when P is split
+      uint32_t pa[NKB][NA], la[NKB][NA];
+#pragma unroll
+      for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+        for (int x = 0; x < NA; ++x) {
+          // x = 0, 1: row lo, keys 2t.. and 8 + 2t..; x = 2, 3: row hi
+          const float v0 = sc[2 * kb + (x & 1)][(x >> 1) * 2];
+          const float v1 = sc[2 * kb + (x & 1)][(x >> 1) * 2 + 1];
+          pa[kb][x] = Elt<T>::from_f2(v0, v1);
+          la[kb][x] = 0u;
+          if (split_p) {
+            const float2 h = Elt<T>::to_f2(pa[kb][x]);
+            la[kb][x] = Elt<T>::from_f2(v0 - h.x, v1 - h.y);
+          }
+        }
+
+      // O += P V; V rows of keys past the range (other data, or stale stage
+      // contents: possibly NaN) are zeroed in the fragments, since 0 * NaN = NaN
+      const bool vpart = nval < kofs + KW;
+#pragma unroll
+      for (int kb = 0; kb < NKB; ++kb) {
+        uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
+        if (vpart) {
+          const int k0 = kofs + kb * 16 + 2 * t;  // ldmatrix.trans: this lane's keys 2t, 2t+1 (+8)
+          mlo = (k0 < nval ? 0x0000ffffu : 0u) | (k0 + 1 < nval ? 0xffff0000u : 0u);
+          mhi = (k0 + 8 < nval ? 0x0000ffffu : 0u) | (k0 + 9 < nval ? 0xffff0000u : 0u);
+        }
+#pragma unroll
+        for (int dp = 0; dp < NNT / 2; ++dp) {
+          uint32_t v0, v1, v2, v3;
+          ldsm_x4_t(vbase + sw_off<D>(kofs + kb * 16 + (mi & 1) * 8 + ri, 2 * dp + (mi >> 1)), v0, v1, v2, v3);
+          v0 &= mlo;
+          v1 &= mhi;
+          v2 &= mlo;
+          v3 &= mhi;
+          Mma<T>::run(o[2 * dp], pa[kb], v0, v1);
+          Mma<T>::run(o[2 * dp + 1], pa[kb], v2, v3);
+          if (split_p) {
+            Mma<T>::run(o[2 * dp], la[kb], v0, v1);
+            Mma<T>::run(o[2 * dp + 1], la[kb], v2, v3);
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[st]);
+    }
+
+    pdl_launch();
+    // ---------------------------------------------------------------- combine the key subsets
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 1);
+    l_lo += __shfl_xor_sync(0xffffffffu, l_lo, 2);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 1);
+    l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
+    asm volatile("bar.sync 1, %0;" ::"n"(THREADS) : "memory");  // stage memory is free from here
+#pragma unroll
+    for (int n = 0; n < NNT; ++n) {
+      *reinterpret_cast<float2*>(&comb_o[(warp * 16 + g) * D + n * 8 + 2 * t]) = make_float2(o[n][0], o[n][1]);
+      *reinterpret_cast<float2*>(&comb_o[(warp * 16 + g + 8) * D + n * 8 + 2 * t]) = make_float2(o[n][2], o[n][3]);
+    }
+    if (t == 0) {
+      comb_m[warp * 16 + g] = m_lo;
+      comb_l[warp * 16 + g] = l_lo;
+      comb_m[warp * 16 + g + 8] = m_hi;
+      comb_l[warp * 16 + g + 8] = l_hi;
+    }
   }
   asm volatile("bar.sync 2, 128;" ::: "memory");
   if (*abort_flag) return;
