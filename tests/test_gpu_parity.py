@@ -604,3 +604,54 @@ def test_consecutive_page_runs(ps, layout):
     kvd = _hnd(w2.kv_cache) if layout == "HND" else None
     o2, l2, _ = run(w2, kv=kvd, kv_layout=layout, decode_chunk_pages=max(1, 256 // ps))
     assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+@pytest.mark.parametrize("G,qo", [(8, 1), (4, 2), (1, 5), (8, 4), (16, 1)],
+                         ids=["rows8_G8", "rows8_G4", "rows5_G1", "rows32", "rows16"])
+@pytest.mark.parametrize("ps", [16, 4])
+def test_decode_launch_shapes_agree(G, qo, ps):
+    """The same small-query items launched one CTA per SM (six stages, more
+    producer warps) and two CTAs per SM (three stages): planned for many SMs
+    and for four, with the decode split fixed so that the items agree.  The
+    outputs are identical bit for bit and match the oracle (row classes 0, 1
+    and 2; TMA and cp.async staging)."""
+    qos = [qo] * 12
+    kvs = [qo + 130 + 97 * i for i in range(12)]
+    w = workloads.make_custom("shape", qos, kvs, 2 * G, 2, 128, ps, dtype=torch.bfloat16, seed=G * 10 + qo)
+    ro, rl = A.attention(w)
+    chunk = max(1, 128 // ps)
+    o1, l1, p1 = run(w, num_sms=1024, decode_chunk_pages=chunk)
+    o2, l2, p2 = run(w, num_sms=4, decode_chunk_pages=chunk)
+    h1, h2 = plan_ref.decode_header(p1.dump()), plan_ref.decode_header(p2.dump())
+    assert h1["n_pre"] == 0 and h1["n_dec"] == h2["n_dec"] and h1["n_dec"] > 4
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+    assert_close(o1, l1, ro, rl, w.dtype, what=f"launch shapes G{G} qo{qo} ps{ps}")
+
+
+def test_back_to_back_runs_chain():
+    """Runs queued back to back on one stream, whose kernels may start before
+    the previous kernel ends (programmatic dependent launch): run 2 reads as
+    its q the out that run 1 writes; run 4 overwrites that buffer right after
+    run 2 and a copy have read it; all runs share the plan's split-KV
+    partial states.  Every result equals the same run made after a full
+    device synchronisation, bit for bit."""
+    w = workloads.mixed(num_decode=24, prefill_len=700, kv_lo=16, kv_hi=3000)
+    plan = pa.Plan(**w.plan_args(), dtype=w.dtype)
+    q, kv = w.q.cuda(), w.kv_cache.cuda()
+    q3 = (w.q * 0.5).cuda()
+    o1, _ = plan.run(q, kv)
+    o2, _ = plan.run(o1, kv)
+    o3, _ = plan.run(q3, kv)
+    o1b = o1.clone()
+    o4, _ = plan.run(q3, kv, out=o1)     # overwrites o1 right after the clone reads it
+    torch.cuda.synchronize()
+    assert plan.device_status() == 0
+    r1, _ = plan.run(q, kv)
+    torch.cuda.synchronize()
+    r2, _ = plan.run(r1.clone(), kv)
+    torch.cuda.synchronize()
+    r3, _ = plan.run(q3, kv)
+    torch.cuda.synchronize()
+    assert torch.equal(o1b, r1)
+    assert torch.equal(o2, r2)
+    assert torch.equal(o3, r3) and torch.equal(o1, r3) and torch.equal(o4, r3)
