@@ -106,7 +106,7 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
       if (!use_tma || jj >= nstage) return 0;
       const int s0j = it.tok0 + jj * kDecTile;
       const int nb = (min(s0j + kDecTile, it.tok1) - s0j + BR - 1) >> br_shift;
-      return lane < nb ? __ldg(p.pages + rq.page_start + ((s0j + lane * BR) >> p.ps_shift)) : 0;
+      return lane < nb ? __ldg(p.pages + it.page_start + ((s0j + lane * BR) >> p.ps_shift)) : 0;
     };
     int pids[3] = {stage_pid(0), stage_pid(1), stage_pid(2)};
     pdl_wait();  // the cache may come from the previous kernel on the stream
@@ -156,7 +156,7 @@ __device__ __forceinline__ void decode_produce(const CUtensorMap& kv_map, const 
           const T* srck = kvb;
           const T* srcv = kvb;
           if (valid) {
-            const KvLoc loc = kv_locate(p.pages, rq.page_start, s0 + t, p.ps_shift);
+            const KvLoc loc = kv_locate(p.pages, it.page_start, s0 + t, p.ps_shift);
             int pid = loc.page;
             if (static_cast<unsigned>(pid) >= static_cast<unsigned>(p.num_pages)) {
               atomicOr(p.status, PA_DEV_BAD_INDEX);

@@ -28,7 +28,7 @@ constexpr int kItemRows = 256;  // packed query rows per prefill work item (two 
 constexpr int kKvTile = 128;  // keys per prefill key tile
 
 struct ReqEntry { int32_t qo_start, qo_len, kv_len, page_start; };
-struct DecItem { int32_t req, kv_head, tok0, tok1, part_row, pad0, pad1, pad2; };
+struct DecItem { int32_t req, kv_head, tok0, tok1, part_row, page_start, pad1, pad2; };  // page_start: req's
 struct PreItem { int32_t req, kv_head, q_tok0, q_ntok, kv_tok0, kv_tok1, part_row, pad0; };
 struct MergeEntry { int32_t out_row0, part_row0, nsplit, split_stride; };
 static_assert(sizeof(DecItem) == 32 && sizeof(PreItem) == 32 && sizeof(MergeEntry) == 16, "layout");

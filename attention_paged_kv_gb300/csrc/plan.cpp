@@ -432,6 +432,7 @@ pagedattn_status build_plan(const PlanInputs& in, HostPlan* hp, std::string* err
   for (size_t j = 0; j < dec.size(); ++j) {
     int32_t* r = blob.data() + off_dec / 4 + 8 * j;
     r[0] = dec[j].req; r[1] = dec[j].kvh; r[2] = dec[j].t0; r[3] = dec[j].t1; r[4] = dec[j].part;
+    r[5] = req[dec[j].req].p0;  // the request's page_start again: one dependent read less for the producer
   }
   for (size_t j = 0; j < pre.size(); ++j) {
     int32_t* r = blob.data() + off_pre / 4 + 8 * j;

@@ -75,7 +75,7 @@ start of the workspace:
     pages[nnz]       copy of kv_page_indices
     req[B + groups][4]  qo_start, qo_len, kv_len, page_start (group g's prefix: entry B + g,
                      qo_len 0, its query tokens' qo_start, the prefix pages after the requests')
-    dec[n_dec][8]    req, kv_head, tok0, tok1, part_row(-1 = direct), 0, 0, 0
+    dec[n_dec][8]    req, kv_head, tok0, tok1, part_row(-1 = direct), page_start of req, 0, 0
     pre[n_pre][8]    req, kv_head, q_tok0, q_ntok, kv_tok0, kv_tok1, part_row, 0
     merge[n][4]      out_row0, part_row0, nsplit, split_stride
 """
@@ -357,7 +357,8 @@ def build(qo_indptr, kv_page_indptr, kv_page_indices, kv_last_page_len, num_qo_h
     for g, (r0, r1, Tg, npp, pstart) in enumerate(groups):  # virtual prefix requests, qo_len 0
         blob[off_req // 4 + 4 * (B + g): off_req // 4 + 4 * (B + g) + 4] = (int(qo_indptr[r0]), 0, npp * ps, pstart)
     for j, it in enumerate(dec):
-        blob[off_dec // 4 + 8 * j: off_dec // 4 + 8 * j + 5] = it[:5]  # words 5..7 stay 0
+        blob[off_dec // 4 + 8 * j: off_dec // 4 + 8 * j + 5] = it[:5]
+        blob[off_dec // 4 + 8 * j + 5] = lens[it[0]][2]  # the request's page_start; words 6, 7 stay 0
     for j, it in enumerate(pre):
         blob[off_pre // 4 + 8 * j: off_pre // 4 + 8 * j + 7] = it
     for j, it in enumerate(merges):
