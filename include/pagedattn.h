@@ -243,7 +243,11 @@ PAGEDATTN_API pagedattn_status pagedattn_workspace_size_cascade(const pagedattn_
  * Launches the prefill kernel (tcgen05 / TMEM), the small-query kernels
  * (decode and requests of qo_len * G <= 32 rows: warp-level MMA, one launch
  * per row class, or the CUDA-core decode kernel) and, when some request was
- * split, the merge kernel, in that order on `stream`.  Allocates nothing and does not synchronise the host.  In-kernel
+ * split, the merge kernel, in that order on `stream`.  Allocates nothing and does not synchronise the host.
+ * The kernels are launched with programmatic stream serialization: each may
+ * begin its set-up while the kernel before it on `stream` finishes, and
+ * waits for that kernel's completion before it reads q, kv_cache or partial
+ * states or writes anything, so stream order holds for every buffer.  In-kernel
  * waits are bounded; a wait that gives up sets PA_DEV_TIMEOUT in the device
  * status word (read it with pagedattn_device_status).  Calls that overlap on
  * the device must use different workspaces (the partial states live there),
