@@ -441,7 +441,8 @@ __global__ void __launch_bounds__(kDecThreads, (NST <= 3 ? 2 : 1))
 // Small-query kernel on the tensor cores (warp-level MMA, m16n8k16, fp32
 // accumulate): decode, and requests of a few query tokens (speculative
 // decoding, small chunks) whose qo_len * G packed (token, head) rows number
-// at most 64.
+// at most 32.  Launches of no more CTAs than SMs run one CTA per SM with six
+// 64-key stages (192 KB in flight); larger ones two CTAs per SM with three.
 //
 // At G query heads per kv head the CUDA-core kernel above needs 2*G MACs per
 // cached element, more than the FP32 pipe sustains at HBM speed once G >= 4;
@@ -466,11 +467,13 @@ __global__ void __launch_bounds__(kDecThreads, (NST <= 3 ? 2 : 1))
 //              fragment (a quad of lanes holds a row), whose exp2 values
 //              become the A fragment of P V directly; ldmatrix.trans feeds V.
 //              O stays in registers; the key subsets are combined at the end.
-// Row classes (template RC): up to 8 and up to 16 rows (RGN 1; fragment rows
-// past R see no keys) and 32 (RGN 2); the first two run the same code and
-// differ only in how the planner groups items.  (64 rows, RGN 4, is never
-// planned: there the warp-level MMA bound the kernel at 43 % of HBM, and the
-// tcgen05 prefill kernel is faster.)  Each row's keys end at its own causal limit.  For requests with
+// Row classes (template RC): up to 8 rows, up to 16 (RGN 1; fragment rows
+// past R see no keys) and 32 (RGN 2).  Class 0 (up to 8 rows) computes the
+// transposed products instead (S^T = K q^T, O^T = V^T P^T: the rows on the
+// MMAs' 8-wide N side, half the MMAs of the direct form, which leaves 8 of
+// 16 M rows idle).  (64 rows, RGN 4, is never planned: there the warp-level
+// MMA bound the kernel at 43 % of HBM, and the tcgen05 prefill kernel is
+// faster.)  Each row's keys end at its own causal limit.  For requests with
 // fewer than 128 keys P is split into hi + lo halves (two MMAs), as in the
 // prefill kernel, so rows that see few keys keep P's rounding out of the
 // output.

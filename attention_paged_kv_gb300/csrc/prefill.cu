@@ -11,14 +11,16 @@
 // ("skips the fully masked out tails", llama.cpp discussion "Pad for prefill
 // stage?").
 //
-// Warp roles (320 threads):
+// Warp roles (352 threads):
 //   warps 0-3  softmax / correction / epilogue of tile A; thread i owns row i
 //              = TMEM lane i, so the online softmax needs no shuffles.
 //   warps 4-7  the same for tile B.
-//   warp 8     producer: TMA loads of the two Q tiles (3-D map over q) and of
-//              each key tile's pages through the page table (4-D map over the
-//              cache, 128-byte swizzle), or cp.async for pages of < 8 slots.
+//   warp 8     K producer: TMA loads of the two Q tiles (3-D map over q) and
+//              of each key tile's K pages through the page table (4-D map
+//              over the cache, 128-byte swizzle), or cp.async for pages of
+//              < 8 slots.
 //   warp 9     MMA issuer (one thread) and TMEM owner.
+//   warp 10    V producer: the same for each key tile's V pages.
 //
 // K and V tiles have separate two-slot rings (four for head_dim 64), so the
 // next K tile loads as soon as both S MMAs have read the slot it reuses.  The
