@@ -330,7 +330,7 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
   // the tensor maps of the last pointers seen are cached in the plan; the
   // launches below use copies taken under the plan's lock, so host threads
   // that run one plan at once never see a half-written map
-  CUtensorMap map_rows, map_sw128, map_q;
+  CUtensorMap map_rows, map_sw128, map_q, map_o;
   {
     std::lock_guard<std::mutex> lock(plan->maps_mu);
     if ((hp.n_pre > 0 || hp.n_dec > 0) && kv_cache != plan->map_kv) {
@@ -350,9 +350,16 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
       if (s != PA_OK) return s;
       plan->map_q_ptr = q;
     }
+    if (hp.n_pre > 0 && out != plan->map_o_ptr) {  // full output tiles leave by TMA stores
+      plan->map_o_ptr = nullptr;
+      pagedattn_status s = pa::encode_q_map(&plan->map_o, hp, out);
+      if (s != PA_OK) return s;
+      plan->map_o_ptr = out;
+    }
     map_rows = plan->map_rows;
     map_sw128 = plan->map_sw128;
     map_q = plan->map_q;
+    map_o = plan->map_o;
   }
   pa::RunArgs a;
   a.hp = &hp;
@@ -364,7 +371,7 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.force_cp_async = plan->force_cp_async;
   if (stage_mask & PA_STAGE_PREFILL) {
-    e = pa::launch_prefill(a, hp.ps >= 8 ? &map_sw128 : nullptr, &map_q);
+    e = pa::launch_prefill(a, hp.ps >= 8 ? &map_sw128 : nullptr, &map_q, &map_o);
     if (e != cudaSuccess) return cuda_err(e, "prefill launch");
   }
   if (stage_mask & PA_STAGE_DECODE) {

@@ -64,7 +64,8 @@ struct RunArgs {
   int force_cp_async;
 };
 
-cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const CUtensorMap* map_q);
+cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const CUtensorMap* map_q,
+                           const CUtensorMap* map_o);
 cudaError_t launch_decode(const RunArgs& a, const CUtensorMap* map_rows);
 cudaError_t launch_merge(const RunArgs& a);
 cudaError_t launch_debug_gather(const RunArgs& a, int32_t* page_out, int32_t* slot_out);
@@ -115,6 +116,8 @@ pagedattn_status cuda_err(cudaError_t e, const char* what);
 // box {box0, 1, box2, 1} (api.cu).
 pagedattn_status encode_kv_map(CUtensorMap* m, const HostPlan& hp, const void* kv, uint32_t box0, uint32_t box2,
                                CUtensorMapSwizzle sw);
+// Tensor map over q, or over out (same shape), viewed as (D, Hq, T), box
+// {64, G, 128 / G}: one 128-row query tile of 64 columns (api.cu).
 pagedattn_status encode_q_map(CUtensorMap* m, const HostPlan& hp, const void* q);
 
 }  // namespace pa
@@ -135,4 +138,6 @@ struct pagedattn_plan_s {
   // tensor map over the last q pointer seen by run() (prefill Q tiles)
   const void* map_q_ptr = nullptr;
   CUtensorMap map_q;
+  const void* map_o_ptr = nullptr;  // the out array of map_o (same box as map_q)
+  CUtensorMap map_o;
 };

@@ -155,7 +155,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 template <typename T, int D, int NT>
 __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-                   const KParams p, const int use_tma) {
+                   const __grid_constant__ CUtensorMap o_map, const KParams p, const int use_tma) {
   using C = PreCfg<D, NT>;
   constexpr int NKB = C::NKB, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
@@ -182,6 +182,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 24);
   volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_slot + 1);
   uint64_t* never = bars + 25;          // test hook: a barrier nothing completes
+  uint64_t* o_st = bars + 26;           // [2] tile x's O staged in shared memory (its 4 warps)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const PreItem it = p.pre[blockIdx.x];
@@ -209,6 +210,8 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     }
     mbar_init(fin, 1);
     mbar_init(never, 1);
+    mbar_init(&o_st[0], 4);
+    mbar_init(&o_st[1], 4);
     *abort_flag = 0;
     mbar_init_fence();
   }
@@ -225,6 +228,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     const int h1 = (C::PRODS == 2 && warp == C::WARP_PROD) ? 1 : 2;
     if (warp == C::WARP_PROD && lane == 0) {
       tma_prefetch_desc(&q_map);
+      tma_prefetch_desc(&o_map);
       if (use_tma) tma_prefetch_desc(&kv_map);
     }
     const int ps = p.ps, sh = p.ps_shift;
@@ -618,8 +622,42 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
         for (int c4 = 0; c4 < D / 32; ++c4)
 #pragma unroll
           for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(o[c4][i]));
+        // a full tile of direct output leaves by TMA stores: O (scaled and
+        // packed) is staged in the tile's Q slot, free since the tile's last
+        // S MMA, as the 128-byte-swizzled box that the out map copies (the
+        // same box as the Q load's); partial tiles and split states are
+        // written row by row
+        const bool tma_out = !partial && (x * TQ + TQ) <= it.q_ntok;
+        if (tma_out) {
+          uint8_t* orow = smem + C::OFF_Q + x * C::Q_BYTES + r * 128;
 #pragma unroll
-        for (int c4 = 0; c4 < D / 32; ++c4) store_chunk(c4, o[c4]);
+          for (int kb = 0; kb < NKB; ++kb)
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const int e = kb * 64 + c * 8;  // the chunk's first column
+              const uint32_t* v = &o[e >> 5][e & 31];
+              uint4 w;
+              w.x = Elt<T>::from_f2(__uint_as_float(v[0]) * inv_l, __uint_as_float(v[1]) * inv_l);
+              w.y = Elt<T>::from_f2(__uint_as_float(v[2]) * inv_l, __uint_as_float(v[3]) * inv_l);
+              w.z = Elt<T>::from_f2(__uint_as_float(v[4]) * inv_l, __uint_as_float(v[5]) * inv_l);
+              w.w = Elt<T>::from_f2(__uint_as_float(v[6]) * inv_l, __uint_as_float(v[7]) * inv_l);
+              *reinterpret_cast<uint4*>(orow + kb * C::BLK + ((c ^ (r & 7)) << 4)) = w;
+            }
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&o_st[x]);
+          if (r == 0 && mbar_wait(&o_st[x], 0, abort_flag, p.status, p.wait_limit)) {
+#pragma unroll
+            for (int kb = 0; kb < NKB; ++kb)
+              tma_store_3d(&o_map, q_addr(x) + kb * C::BLK, kb * 64, it.kv_head * G,
+                           rq.qo_start + it.q_tok0 + x * TQ);
+            tma_store_commit();
+            tma_store_wait_read();  // the Q slot is read before the CTA's memory goes away
+          }
+        } else {
+#pragma unroll
+          for (int c4 = 0; c4 < D / 32; ++c4) store_chunk(c4, o[c4]);
+        }
       } else {
 #pragma unroll
         for (int c4 = 0; c4 < D / 32; ++c4) {
@@ -653,25 +691,25 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
 
 template <typename T, int D, int NT>
 cudaError_t launch_prefill_t(const RunArgs& a, const CUtensorMap* kv_map, const CUtensorMap* q_map,
-                             const KParams& kp, int use_tma) {
+                             const CUtensorMap* o_map, const KParams& kp, int use_tma) {
   using C = PreCfg<D, NT>;
   static std::atomic<uint64_t> attr_set{0};
   cudaError_t e = set_smem_once(attr_set, reinterpret_cast<const void*>(prefill_kernel<T, D, NT>), C::SMEM);
   if (e != cudaSuccess) return e;
   return launch_pdl(prefill_kernel<T, D, NT>, unsigned(a.hp->n_pre), unsigned(C::THREADS), size_t(C::SMEM), a.stream,
-                    *kv_map, *q_map, kp, use_tma);
+                    *kv_map, *q_map, *o_map, kp, use_tma);
 }
 
 template <typename T>
 cudaError_t launch_prefill_dt(const RunArgs& a, const CUtensorMap* kv_map, const CUtensorMap* q_map,
-                              const KParams& kp, int use_tma) {
+                              const CUtensorMap* o_map, const KParams& kp, int use_tma) {
   const bool one = a.hp->pre_tiles == 1;
   switch (a.hp->D) {
-    case 64: return one ? launch_prefill_t<T, 64, 1>(a, kv_map, q_map, kp, use_tma)
-                        : launch_prefill_t<T, 64, 2>(a, kv_map, q_map, kp, use_tma);
-    case 128: return one ? launch_prefill_t<T, 128, 1>(a, kv_map, q_map, kp, use_tma)
-                         : launch_prefill_t<T, 128, 2>(a, kv_map, q_map, kp, use_tma);
-    case 256: return one ? launch_prefill_t<T, 256, 1>(a, kv_map, q_map, kp, use_tma) : cudaErrorInvalidValue;
+    case 64: return one ? launch_prefill_t<T, 64, 1>(a, kv_map, q_map, o_map, kp, use_tma)
+                        : launch_prefill_t<T, 64, 2>(a, kv_map, q_map, o_map, kp, use_tma);
+    case 128: return one ? launch_prefill_t<T, 128, 1>(a, kv_map, q_map, o_map, kp, use_tma)
+                         : launch_prefill_t<T, 128, 2>(a, kv_map, q_map, o_map, kp, use_tma);
+    case 256: return one ? launch_prefill_t<T, 256, 1>(a, kv_map, q_map, o_map, kp, use_tma) : cudaErrorInvalidValue;
     default: return cudaErrorInvalidValue;
   }
 }
@@ -680,7 +718,8 @@ cudaError_t launch_prefill_dt(const RunArgs& a, const CUtensorMap* kv_map, const
 
 KParams make_params(const RunArgs& a);
 
-cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const CUtensorMap* map_q) {
+cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const CUtensorMap* map_q,
+                           const CUtensorMap* map_o) {
   if (a.hp->n_pre == 0) return cudaSuccess;
   KParams kp = make_params(a);
   kp.n_items = a.hp->n_pre;
@@ -688,8 +727,8 @@ cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const
   CUtensorMap dummy;
   memset(&dummy, 0, sizeof(dummy));
   const CUtensorMap* m = use_tma ? map_sw128 : &dummy;
-  return a.hp->dtype == PA_BF16 ? launch_prefill_dt<__nv_bfloat16>(a, m, map_q, kp, use_tma)
-                                 : launch_prefill_dt<__half>(a, m, map_q, kp, use_tma);
+  return a.hp->dtype == PA_BF16 ? launch_prefill_dt<__nv_bfloat16>(a, m, map_q, map_o, kp, use_tma)
+                                 : launch_prefill_dt<__half>(a, m, map_q, map_o, kp, use_tma);
 }
 
 }  // namespace pa
