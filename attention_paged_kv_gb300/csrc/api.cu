@@ -81,12 +81,12 @@ pagedattn_status encode_kv_map(CUtensorMap* m, const pa::HostPlan& hp, const voi
 
 // 3-D view of q: (D, Hq, T), innermost first; box {64, G, 128 / G}: one
 // 128-row tile of packed (token, head) rows of one kv head, 128-byte swizzle.
-pagedattn_status encode_q_map(CUtensorMap* m, const pa::HostPlan& hp, const void* q) {
+pagedattn_status encode_q_map(CUtensorMap* m, const pa::HostPlan& hp, const void* q, uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return set_err(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
   const cuuint64_t dims[3] = {cuuint64_t(hp.D), cuuint64_t(hp.Hq), cuuint64_t(hp.T)};
   const cuuint64_t strides[2] = {cuuint64_t(hp.D) * 2, cuuint64_t(hp.Hq) * hp.D * 2};
-  const cuuint32_t box[3] = {64, cuuint32_t(hp.G), cuuint32_t(pa::kQRows / hp.G)};
+  const cuuint32_t box[3] = {64, cuuint32_t(hp.G), cuuint32_t(box_rows / hp.G)};
   const cuuint32_t estr[3] = {1, 1, 1};
   const CUtensorMapDataType dt =
       hp.dtype == PA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
@@ -330,7 +330,7 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
   // the tensor maps of the last pointers seen are cached in the plan; the
   // launches below use copies taken under the plan's lock, so host threads
   // that run one plan at once never see a half-written map
-  CUtensorMap map_rows, map_sw128, map_q, map_o;
+  CUtensorMap map_rows, map_sw128, map_q, map_o[2];
   {
     std::lock_guard<std::mutex> lock(plan->maps_mu);
     if ((hp.n_pre > 0 || hp.n_dec > 0) && kv_cache != plan->map_kv) {
@@ -352,14 +352,16 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
     }
     if (hp.n_pre > 0 && out != plan->map_o_ptr) {  // full output tiles leave by TMA stores
       plan->map_o_ptr = nullptr;
-      pagedattn_status s = pa::encode_q_map(&plan->map_o, hp, out);
+      pagedattn_status s = pa::encode_q_map(&plan->map_o[0], hp, out);
+      if (s == PA_OK) s = pa::encode_q_map(&plan->map_o[1], hp, out, 32);
       if (s != PA_OK) return s;
       plan->map_o_ptr = out;
     }
     map_rows = plan->map_rows;
     map_sw128 = plan->map_sw128;
     map_q = plan->map_q;
-    map_o = plan->map_o;
+    map_o[0] = plan->map_o[0];
+    map_o[1] = plan->map_o[1];
   }
   pa::RunArgs a;
   a.hp = &hp;
@@ -371,7 +373,7 @@ pagedattn_status pagedattn_run_stages(pagedattn_plan_t plan, const void* q, cons
   a.stream = reinterpret_cast<cudaStream_t>(stream);
   a.force_cp_async = plan->force_cp_async;
   if (stage_mask & PA_STAGE_PREFILL) {
-    e = pa::launch_prefill(a, hp.ps >= 8 ? &map_sw128 : nullptr, &map_q, &map_o);
+    e = pa::launch_prefill(a, hp.ps >= 8 ? &map_sw128 : nullptr, &map_q, map_o);
     if (e != cudaSuccess) return cuda_err(e, "prefill launch");
   }
   if (stage_mask & PA_STAGE_DECODE) {

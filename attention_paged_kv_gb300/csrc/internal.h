@@ -65,7 +65,7 @@ struct RunArgs {
 };
 
 cudaError_t launch_prefill(const RunArgs& a, const CUtensorMap* map_sw128, const CUtensorMap* map_q,
-                           const CUtensorMap* map_o);
+                           const CUtensorMap* map_o);  // map_o: [2], 128-row and 32-row boxes over out
 cudaError_t launch_decode(const RunArgs& a, const CUtensorMap* map_rows);
 cudaError_t launch_merge(const RunArgs& a);
 cudaError_t launch_debug_gather(const RunArgs& a, int32_t* page_out, int32_t* slot_out);
@@ -118,7 +118,7 @@ pagedattn_status encode_kv_map(CUtensorMap* m, const HostPlan& hp, const void* k
                                CUtensorMapSwizzle sw);
 // Tensor map over q, or over out (same shape), viewed as (D, Hq, T), box
 // {64, G, 128 / G}: one 128-row query tile of 64 columns (api.cu).
-pagedattn_status encode_q_map(CUtensorMap* m, const HostPlan& hp, const void* q);
+pagedattn_status encode_q_map(CUtensorMap* m, const HostPlan& hp, const void* q, uint32_t box_rows = 128);
 
 }  // namespace pa
 
@@ -138,6 +138,6 @@ struct pagedattn_plan_s {
   // tensor map over the last q pointer seen by run() (prefill Q tiles)
   const void* map_q_ptr = nullptr;
   CUtensorMap map_q;
-  const void* map_o_ptr = nullptr;  // the out array of map_o (same box as map_q)
-  CUtensorMap map_o;
+  const void* map_o_ptr = nullptr;  // the out array of map_o: 128-row boxes (as map_q), then 32-row boxes
+  CUtensorMap map_o[2];
 };

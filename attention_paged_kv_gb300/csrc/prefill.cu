@@ -155,7 +155,8 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 template <typename T, int D, int NT>
 __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     prefill_kernel(const __grid_constant__ CUtensorMap kv_map, const __grid_constant__ CUtensorMap q_map,
-                   const __grid_constant__ CUtensorMap o_map, const KParams p, const int use_tma) {
+                   const __grid_constant__ CUtensorMap o_map, const __grid_constant__ CUtensorMap o32_map,
+                   const KParams p, const int use_tma) {
   using C = PreCfg<D, NT>;
   constexpr int NKB = C::NKB, NST = C::NST;
   extern __shared__ uint8_t smem_raw[];
@@ -229,6 +230,7 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
     if (warp == C::WARP_PROD && lane == 0) {
       tma_prefetch_desc(&q_map);
       tma_prefetch_desc(&o_map);
+      tma_prefetch_desc(&o32_map);
       if (use_tma) tma_prefetch_desc(&kv_map);
     }
     const int ps = p.ps, sh = p.ps_shift;
@@ -622,35 +624,53 @@ __global__ void __launch_bounds__(PreCfg<D, NT>::THREADS, NT == 1 ? 2 : 1)
         for (int c4 = 0; c4 < D / 32; ++c4)
 #pragma unroll
           for (int i = 0; i < 32; ++i) asm volatile("" : "+r"(o[c4][i]));
-        // a full tile of direct output leaves by TMA stores: O (scaled and
-        // packed) is staged in the tile's Q slot, free since the tile's last
-        // S MMA, as the 128-byte-swizzled box that the out map copies (the
-        // same box as the Q load's); partial tiles and split states are
-        // written row by row
-        const bool tma_out = !partial && (x * TQ + TQ) <= it.q_ntok;
-        if (tma_out) {
-          uint8_t* orow = smem + C::OFF_Q + x * C::Q_BYTES + r * 128;
+        // direct output leaves by TMA stores: O (scaled and packed) is staged
+        // in the tile's Q slot, free since the tile's last S MMA, as the
+        // 128-byte-swizzled rows that the out maps copy -- a full tile as one
+        // 128-row box (the Q load's box), a partial one as the 32-row boxes
+        // its valid rows fill, the rows after those copied out of the staged
+        // tile row by row; split states are written row by row
+        const int vrows = partial ? 0 : min(kQRows, (it.q_ntok - x * TQ) << p.g_shift);
+        const int srows = vrows & ~31;  // rows the TMA stores carry
+        if (srows > 0) {
+          if (r < srows) {
+            uint8_t* orow = smem + C::OFF_Q + x * C::Q_BYTES + r * 128;
 #pragma unroll
-          for (int kb = 0; kb < NKB; ++kb)
+            for (int kb = 0; kb < NKB; ++kb)
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-              const int e = kb * 64 + c * 8;  // the chunk's first column
-              const uint32_t* v = &o[e >> 5][e & 31];
-              uint4 w;
-              w.x = Elt<T>::from_f2(__uint_as_float(v[0]) * inv_l, __uint_as_float(v[1]) * inv_l);
-              w.y = Elt<T>::from_f2(__uint_as_float(v[2]) * inv_l, __uint_as_float(v[3]) * inv_l);
-              w.z = Elt<T>::from_f2(__uint_as_float(v[4]) * inv_l, __uint_as_float(v[5]) * inv_l);
-              w.w = Elt<T>::from_f2(__uint_as_float(v[6]) * inv_l, __uint_as_float(v[7]) * inv_l);
-              *reinterpret_cast<uint4*>(orow + kb * C::BLK + ((c ^ (r & 7)) << 4)) = w;
-            }
+              for (int c = 0; c < 8; ++c) {
+                const int e = kb * 64 + c * 8;  // the chunk's first column
+                const uint32_t* v = &o[e >> 5][e & 31];
+                uint4 w;
+                w.x = Elt<T>::from_f2(__uint_as_float(v[0]) * inv_l, __uint_as_float(v[1]) * inv_l);
+                w.y = Elt<T>::from_f2(__uint_as_float(v[2]) * inv_l, __uint_as_float(v[3]) * inv_l);
+                w.z = Elt<T>::from_f2(__uint_as_float(v[4]) * inv_l, __uint_as_float(v[5]) * inv_l);
+                w.w = Elt<T>::from_f2(__uint_as_float(v[6]) * inv_l, __uint_as_float(v[7]) * inv_l);
+                *reinterpret_cast<uint4*>(orow + kb * C::BLK + ((c ^ (r & 7)) << 4)) = w;
+              }
+          } else {  // the partial tile's last rows, row by row
+#pragma unroll
+            for (int c4 = 0; c4 < D / 32; ++c4) store_chunk(c4, o[c4]);
+          }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&o_st[x]);
           if (r == 0 && mbar_wait(&o_st[x], 0, abort_flag, p.status, p.wait_limit)) {
+            const int tok0 = rq.qo_start + it.q_tok0 + x * TQ;
+            if (srows == kQRows) {
 #pragma unroll
-            for (int kb = 0; kb < NKB; ++kb)
-              tma_store_3d(&o_map, q_addr(x) + kb * C::BLK, kb * 64, it.kv_head * G,
-                           rq.qo_start + it.q_tok0 + x * TQ);
+              for (int kb = 0; kb < NKB; ++kb)
+                tma_store_3d(&o_map, q_addr(x) + kb * C::BLK, kb * 64, it.kv_head * G, tok0);
+            } else {
+#pragma unroll
+              for (int b = 0; b < 3; ++b)
+                if (b < (srows >> 5)) {
+#pragma unroll
+                  for (int kb = 0; kb < NKB; ++kb)
+                    tma_store_3d(&o32_map, q_addr(x) + kb * C::BLK + b * 32 * 128, kb * 64, it.kv_head * G,
+                                 tok0 + ((b * 32) >> p.g_shift));
+                }
+            }
             tma_store_commit();
             tma_store_wait_read();  // the Q slot is read before the CTA's memory goes away
           }
@@ -693,11 +713,12 @@ template <typename T, int D, int NT>
 cudaError_t launch_prefill_t(const RunArgs& a, const CUtensorMap* kv_map, const CUtensorMap* q_map,
                              const CUtensorMap* o_map, const KParams& kp, int use_tma) {
   using C = PreCfg<D, NT>;
+  // o_map[0]: 128-row boxes over out; o_map[1]: 32-row boxes
   static std::atomic<uint64_t> attr_set{0};
   cudaError_t e = set_smem_once(attr_set, reinterpret_cast<const void*>(prefill_kernel<T, D, NT>), C::SMEM);
   if (e != cudaSuccess) return e;
   return launch_pdl(prefill_kernel<T, D, NT>, unsigned(a.hp->n_pre), unsigned(C::THREADS), size_t(C::SMEM), a.stream,
-                    *kv_map, *q_map, *o_map, kp, use_tma);
+                    *kv_map, *q_map, o_map[0], o_map[1], kp, use_tma);
 }
 
 template <typename T>
