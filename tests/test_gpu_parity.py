@@ -655,3 +655,21 @@ def test_back_to_back_runs_chain():
     assert torch.equal(o1b, r1)
     assert torch.equal(o2, r2)
     assert torch.equal(o3, r3) and torch.equal(o1, r3) and torch.equal(o4, r3)
+
+
+@pytest.mark.parametrize("G", [1, 4, 16])
+@pytest.mark.parametrize("q_tiles", [1, 2])
+def test_output_tiles_every_fill(G, q_tiles):
+    """Prefill output tiles filled to every row count the epilogue treats
+    apart: fewer than 32 valid rows (written row by row), whole 32-row boxes
+    plus a remainder, and full 128-row tiles (TMA stores), in tile A and in
+    tile B of two-tile items; each against the oracle."""
+    tq = 128 // G
+    qos = sorted({max(1, n) for n in (tq // 4 - 1, tq // 4, tq // 4 + 1, tq // 2, 3 * tq // 4 + 1, tq - 1, tq,
+                                      tq + 1, tq + tq // 4, 2 * tq - 1, 2 * tq)})
+    kvs = [q + 70 for q in qos]
+    w = workloads.make_custom("fill", qos, kvs, 2 * G, 2, 128, 16, dtype=torch.bfloat16, seed=G + q_tiles)
+    ro, rl = A.attention(w)
+    out, lse, plan = run(w, prefill_q_tiles=q_tiles, force_prefill=True)
+    assert plan_ref.decode_header(plan.dump())["n_pre"] > 0
+    assert_close(out, lse, ro, rl, w.dtype, what=f"output tiles G{G} q_tiles {q_tiles}")
